@@ -1,0 +1,54 @@
+"""Named attention workloads and the video -> token-grid rule.
+
+The token grid follows the gojay.top "Wan2.1" reading, *DiT backbone* and
+*Wan-VAE*: the VAE keeps the first frame and compresses the remaining ones 4x
+in time and 8x8 in space, and the DiT patchifies the latent with a (1, 2, 2)
+patch, so a video of 1+T frames at H x W becomes a grid of
+(1 + T/4) x H/16 x W/16 tokens. Model shapes come from the *⑥ 1.3B vs 14B*
+config table of the same page (dim 1536 / 12 heads and 5120 / 40 heads, so a
+head is 128 wide; text conditioning of at most 512 umT5 tokens).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+
+def latent_grid(frames: int, height: int, width: int):
+    """(F, Hp, Wp) token grid of a video of ``frames`` = 1 + T frames."""
+    if frames < 1 or (frames - 1) % 4:
+        raise ValueError("frames must be 1 + 4k")
+    if height % 16 or width % 16:
+        raise ValueError("height and width must be multiples of 16")
+    return 1 + (frames - 1) // 4, height // 16, width // 16
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    kind: str            # "self_fwd", "cross_fwd" or "self_fwd_bwd"
+    B: int
+    grid: tuple          # (F, Hp, Wp) of the queries
+    H: int
+    d: int = 128
+    Lk: int = 0          # cross-attention text keys (allocated length)
+    kv_len_range: tuple = (16, 512)
+
+    @property
+    def L(self) -> int:
+        F, Hp, Wp = self.grid
+        return F * Hp * Wp
+
+    def flops(self) -> float:
+        """4*B*H*Lq*Lk*d forward; the backward counts 2.5x that on top."""
+        lk = self.Lk if self.kind == "cross_fwd" else self.L
+        f = 4.0 * self.B * self.H * self.L * lk * self.d
+        return f * 3.5 if self.kind == "self_fwd_bwd" else f
+
+
+WORKLOADS = {
+    "tiny_3x8x8_h2": Workload("tiny_3x8x8_h2", "self_fwd", 1, (3, 8, 8), 2),
+    "wan1.3b_480p_self_fwd": Workload("wan1.3b_480p_self_fwd", "self_fwd", 1, latent_grid(81, 480, 832), 12),
+    "wan14b_720p_cross_fwd": Workload("wan14b_720p_cross_fwd", "cross_fwd", 2, latent_grid(81, 720, 1280), 40, Lk=512),
+    "wan14b_720p_self_fwd": Workload("wan14b_720p_self_fwd", "self_fwd", 1, latent_grid(81, 720, 1280), 40),
+    "train_64x64x64_fwd_bwd": Workload("train_64x64x64_fwd_bwd", "self_fwd_bwd", 1, (64, 64, 64), 12),
+}

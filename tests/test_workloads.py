@@ -1,0 +1,38 @@
+"""Workload shapes against the shapes the pages print (tests/golden)."""
+import json
+import os
+
+import pytest
+
+from long_sequence_attention_02_b300 import workloads
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "video_token_grids.json")))
+
+
+@pytest.mark.parametrize("case", GOLD["cases"])
+def test_latent_grid(case):
+    g = workloads.latent_grid(case["frames"], case["height"], case["width"])
+    assert list(g) == case["grid"]
+    assert g[0] * g[1] * g[2] == case["tokens"]
+
+
+@pytest.mark.parametrize("m", GOLD["models"])
+def test_head_dim(m):
+    assert m["dim"] // m["heads"] == m["head_dim"] == 128
+
+
+def test_named_workloads():
+    w = workloads.WORKLOADS
+    assert w["wan1.3b_480p_self_fwd"].L == 32760 and w["wan1.3b_480p_self_fwd"].H == 12
+    assert w["wan14b_720p_self_fwd"].L == 75600 and w["wan14b_720p_self_fwd"].H == 40
+    assert w["wan14b_720p_cross_fwd"].Lk == GOLD["text_tokens_max"]
+    assert w["train_64x64x64_fwd_bwd"].L == 262144
+    assert w["tiny_3x8x8_h2"].L == 192
+    assert w["wan14b_720p_self_fwd"].flops() == pytest.approx(1.1705e14, rel=1e-4)
+
+
+def test_bad_video_shapes():
+    with pytest.raises(ValueError):
+        workloads.latent_grid(80, 480, 832)
+    with pytest.raises(ValueError):
+        workloads.latent_grid(81, 480, 830)
