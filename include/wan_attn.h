@@ -1,0 +1,158 @@
+/*
+ * wan_attn.h - C ABI of the B300 (sm_103a) attention library for Wan-style
+ * video diffusion transformers.
+ *
+ * What the library computes (sources are the web pages about the Wan report,
+ * arXiv 2503.20314, cited by page and section):
+ *   - full, non-causal spatio-temporal self-attention over all latent tokens
+ *     ("Wan Team, Alibaba (2025)" anthology note, Key takeaways; ctol.digital
+ *     article, Engineering the Core);
+ *   - 3D RoPE on Q and K with temporal / height / width bands (gojay.top
+ *     "Wan2.1" paper reading, sections 费曼一分钟 and DiT 块);
+ *   - tokens of a (1,2,2)-patchified latent grid, L = F * Hp * Wp (same page,
+ *     DiT backbone);
+ *   - cross-attention from video tokens to at most 512 umT5 text tokens (same
+ *     page, config table ⑥ 1.3B vs 14B; aipaper.jasonlin.tech summary, Key
+ *     contributions);
+ *   - the backward pass used by rectified-flow training (gojay.top page,
+ *     section 3 Training).
+ * The pages fix no constants beyond these; the library's readings are: RoPE
+ * pairs are adjacent dims (2j, 2j+1); the t, h, w bands are contiguous, of
+ * widths d - 4*(d/6), 2*(d/6), 2*(d/6) (44/42/42 at d = 128); pair j of a band
+ * of width w turns by pos * theta^(-2j/w); positions are the 0-based grid
+ * coordinates; token l = (t*Hp + h)*Wp + w; logits are scale * <q_rot, k_rot>;
+ * LSE is the natural log-sum-exp of the scaled logits.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors Q, K, V, O, dO, dQ, dK, dV are bf16 (raw 16-bit storage), layout
+ *     [B, L, H, head_dim], contiguous, head_dim innermost. LSE is fp32 [B, H, L].
+ *   - Every pointer argument except `tables`-free ones named below is a DEVICE
+ *     pointer, 16-byte aligned, owned by the caller. The library never
+ *     allocates or frees on these paths; outputs must not alias inputs.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). All work is enqueued asynchronously on it; a return of WAN_OK
+ *     means the work was launched, not that it finished.
+ *   - Only head_dim == 128 and devices of compute capability 10.3 are
+ *     supported (WAN_ERR_UNSUPPORTED otherwise).
+ *   - Arguments are checked on the host before anything is enqueued; on any
+ *     error nothing is launched. A device-side bounded wait that expires is
+ *     reported later through wan_get_device_status().
+ */
+#ifndef WAN_ATTN_H
+#define WAN_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  WAN_OK = 0,
+  WAN_ERR_INVALID = 1,     /* null pointer, bad size, misalignment, small workspace */
+  WAN_ERR_UNSUPPORTED = 2, /* head_dim != 128, or the device is not sm_103 */
+  WAN_ERR_CUDA = 3,        /* a CUDA call or launch failed */
+  WAN_ERR_TIMEOUT = 4      /* a device-side bounded wait expired (reported by wan_get_device_status) */
+};
+
+enum { WAN_OP_FWD = 0, WAN_OP_BWD = 1 };
+
+/* Latent token grid: F latent frames x Hp x Wp patches, L = F * Hp * Wp. */
+typedef struct {
+  int F, Hp, Wp;
+} wan_grid_t;
+
+/* Human-readable name of a status code (static string). */
+const char* wan_status_str(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int wan_version(void);
+
+/*
+ * 3D RoPE tables (gojay.top "Wan2.1" reading, 费曼一分钟 / DiT 块: 3D RoPE).
+ * Bytes needed for the tables of grid g: (F*nt + Hp*nh + Wp*nw) * 8 with
+ * nt, nh, nw the rotary pairs of the t, h, w bands (22, 21, 21 at d = 128).
+ * Returns 0 for an invalid grid or head_dim.
+ */
+size_t wan_rope3d_tables_size(wan_grid_t g, int head_dim);
+
+/*
+ * Fill `tables_dev` (device, wan_rope3d_tables_size bytes) with float2
+ * {cos, sin} of pos * theta^(-2j/w) for every position of each axis, computed
+ * in double precision on the host and rounded to fp32: first the t table
+ * [F][nt], then h [Hp][nh], then w [Wp][nw]. The copy is enqueued on
+ * `stream`; the host staging buffer is released before return.
+ */
+int wan_rope3d_tables(wan_grid_t g, int head_dim, double theta, float* tables_dev, void* stream);
+
+/*
+ * Workspace bytes for op WAN_OP_FWD (self-attention forward: RoPE'd keys) or
+ * WAN_OP_BWD (backward: rotated Q and K, the fp32 dQ accumulator and the row
+ * dot products D = rowsum(dO * O)).
+ */
+size_t wan_attn_workspace_size(int op, int B, wan_grid_t g, int H, int head_dim);
+
+/*
+ * Self-attention forward with 3D RoPE (anthology note, Key takeaways: full
+ * spatio-temporal self-attention; gojay.top reading, DiT 块: 3D RoPE).
+ *   q, k, v : [B, L, H, 128] bf16 inputs (pre-RoPE q and k)
+ *   o       : [B, L, H, 128] bf16 output, softmax(scale * q_rot k_rot^T) v
+ *   lse     : [B, H, L] fp32 output, natural log-sum-exp of each row (may be NULL)
+ *   tables  : device tables from wan_rope3d_tables for the same grid/head_dim
+ *   scale   : logit scale (1/sqrt(128) for the Wan models)
+ *   workspace, ws_bytes : device scratch of at least wan_attn_workspace_size(WAN_OP_FWD, ...)
+ * B == 0 is a no-op returning WAN_OK.
+ */
+int wan_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g, int H,
+                 int head_dim, const float* tables, float scale, void* workspace, size_t ws_bytes,
+                 void* stream);
+
+/*
+ * Cross-attention forward, video queries to padded text keys, no RoPE
+ * (gojay.top reading, DiT backbone: text enters through cross-attention;
+ * config table: umT5 with 512 tokens).
+ *   q       : [B, Lq, H, 128] bf16, Lq = F * Hp * Wp of grid g
+ *   k, v    : [B, Lk, H, 128] bf16, 1 <= Lk <= 512
+ *   kv_lens : device int32 [B] valid key counts, or NULL for all Lk valid.
+ *             Values are clamped to [0, Lk] on the device; a row with no
+ *             valid key gets O = 0 and LSE = -inf.
+ *   o, lse  : outputs as for wan_attn_fwd (lse may be NULL).
+ */
+int wan_xattn_fwd(const void* q, const void* k, const void* v, const int32_t* kv_lens, int Lk, void* o,
+                  float* lse, int B, wan_grid_t g, int H, int head_dim, float scale, void* stream);
+
+/*
+ * Self-attention backward with 3D RoPE (gojay.top reading, 3 Training: the
+ * rectified-flow step needs gradients through attention).
+ *   q, k, v, o, lse : forward inputs and outputs (lse from wan_attn_fwd)
+ *   dout            : [B, L, H, 128] bf16 upstream gradient
+ *   dq, dk, dv      : [B, L, H, 128] bf16 gradients w.r.t. the pre-RoPE q, k and v
+ *   workspace       : at least wan_attn_workspace_size(WAN_OP_BWD, ...) bytes
+ * dQ is accumulated with fp32 atomics, so it is reproducible only to rounding.
+ */
+int wan_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int B, wan_grid_t g, int H, int head_dim, const float* tables,
+                 float scale, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, then return and clear the device error word of the
+ * current device: WAN_OK, or WAN_ERR_TIMEOUT if a kernel gave up a bounded
+ * wait since the last call (its outputs are then undefined), or WAN_ERR_CUDA
+ * if the synchronisation itself failed.
+ */
+int wan_get_device_status(void* stream);
+
+/*
+ * Test hook (not for production use): make the next `count` attention kernel
+ * launches on this device skip one producer arrival so that their consumers'
+ * bounded waits expire after `timeout_ms`, exercising the timeout path without
+ * faulting. count = 0 restores normal operation.
+ */
+int wan_debug_inject_stall(int count, int timeout_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WAN_ATTN_H */

@@ -1,0 +1,243 @@
+// C ABI of the library: argument checks, workspace sizing, RoPE tables, the
+// device error word and launches. See include/wan_attn.h for the contract.
+#include <climits>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.cuh"
+#include "wan_attn.h"
+
+namespace {
+
+using wan::kHeadDim;
+
+__device__ int g_wan_device_error;  // one per device that loads the library
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;  // 4 s per device-side wait
+
+struct DeviceState {
+  bool probed = false;
+  bool supported = false;
+  int* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+int g_stall_launches = 0;
+uint64_t g_stall_timeout_ns = 0;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int grid_tokens(wan_grid_t g, long long* L) {
+  if (g.F <= 0 || g.Hp <= 0 || g.Wp <= 0) return WAN_ERR_INVALID;
+  const long long l = (long long)g.F * g.Hp * g.Wp;
+  if (l > INT_MAX) return WAN_ERR_INVALID;
+  *L = l;
+  return WAN_OK;
+}
+
+// Shape checks shared by the attention entry points (host only, no CUDA call).
+int check_shapes(int B, long long L, int H, int head_dim) {
+  if (B < 0 || H <= 0 || B > 65535 || H > 65535) return WAN_ERR_INVALID;
+  if (head_dim != kHeadDim) return WAN_ERR_UNSUPPORTED;
+  if ((unsigned long long)L * (unsigned long long)H >= (1ull << 31)) return WAN_ERR_INVALID;
+  return WAN_OK;
+}
+
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return WAN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return WAN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.probed) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return WAN_ERR_CUDA;
+    st.supported = (major == 10 && minor == 3);
+    if (st.supported) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_wan_device_error) != cudaSuccess) return WAN_ERR_CUDA;
+      st.err = static_cast<int*>(p);
+    }
+    st.probed = true;
+  }
+  if (!st.supported) return WAN_ERR_UNSUPPORTED;
+  *out = &st;
+  return WAN_OK;
+}
+
+wan::LaunchCommon launch_common(const DeviceState& st) {
+  wan::LaunchCommon lc;
+  lc.err = st.err;
+  lc.timeout_ns = kDefaultTimeoutNs;
+  lc.stall = 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_stall_launches > 0) {
+    --g_stall_launches;
+    lc.stall = 1;
+    lc.timeout_ns = g_stall_timeout_ns;
+  }
+  return lc;
+}
+
+wan::RopeTables split_tables(const float* tables, wan_grid_t g) {
+  wan::RopeTables t;
+  const float2* base = reinterpret_cast<const float2*>(tables);
+  t.t = base;
+  t.h = base + (size_t)g.F * wan::kPairsT;
+  t.w = t.h + (size_t)g.Hp * wan::kPairsH;
+  return t;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+const char* wan_status_str(int status) {
+  switch (status) {
+    case WAN_OK: return "WAN_OK";
+    case WAN_ERR_INVALID: return "WAN_ERR_INVALID: invalid argument";
+    case WAN_ERR_UNSUPPORTED: return "WAN_ERR_UNSUPPORTED: head_dim or device not supported";
+    case WAN_ERR_CUDA: return "WAN_ERR_CUDA: CUDA call or launch failed";
+    case WAN_ERR_TIMEOUT: return "WAN_ERR_TIMEOUT: device-side wait expired";
+    default: return "unknown wan status";
+  }
+}
+
+int wan_version(void) { return 100; }
+
+size_t wan_rope3d_tables_size(wan_grid_t g, int head_dim) {
+  long long L = 0;
+  if (grid_tokens(g, &L) != WAN_OK || head_dim != kHeadDim) return 0;
+  return ((size_t)g.F * wan::kPairsT + (size_t)g.Hp * wan::kPairsH + (size_t)g.Wp * wan::kPairsW) * 2 *
+         sizeof(float);
+}
+
+int wan_rope3d_tables(wan_grid_t g, int head_dim, double theta, float* tables_dev, void* stream) {
+  long long L = 0;
+  if (grid_tokens(g, &L) != WAN_OK) return WAN_ERR_INVALID;
+  if (head_dim != kHeadDim) return WAN_ERR_UNSUPPORTED;
+  if (tables_dev == nullptr || !(theta > 1.0) || !std::isfinite(theta)) return WAN_ERR_INVALID;
+  // Bands t, h, w of widths 44, 42, 42: pair j of a band of width w turns by
+  // pos * theta^(-2j / w), evaluated in double precision.
+  const int widths[3] = {2 * wan::kPairsT, 2 * wan::kPairsH, 2 * wan::kPairsW};
+  const int npos[3] = {g.F, g.Hp, g.Wp};
+  std::vector<float> host;
+  host.reserve(wan_rope3d_tables_size(g, head_dim) / sizeof(float));
+  for (int ax = 0; ax < 3; ++ax) {
+    const int pairs = widths[ax] / 2;
+    for (int pos = 0; pos < npos[ax]; ++pos)
+      for (int j = 0; j < pairs; ++j) {
+        const double omega = std::pow(theta, -2.0 * j / widths[ax]);
+        const double ang = (double)pos * omega;
+        host.push_back((float)std::cos(ang));
+        host.push_back((float)std::sin(ang));
+      }
+  }
+  cudaError_t e = cudaMemcpyAsync(tables_dev, host.data(), host.size() * sizeof(float), cudaMemcpyHostToDevice,
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+size_t wan_attn_workspace_size(int op, int B, wan_grid_t g, int H, int head_dim) {
+  long long L = 0;
+  if (grid_tokens(g, &L) != WAN_OK || check_shapes(B, L, H, head_dim) != WAN_OK) return 0;
+  if (op == WAN_OP_FWD) return round_up((size_t)B * L * H * kHeadDim * 2, 256);
+  if (op == WAN_OP_BWD) return wan::attn_bwd_workspace_bytes(B, (int)L, H);
+  return 0;
+}
+
+int wan_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g, int H,
+                 int head_dim, const float* tables, float scale, void* workspace, size_t ws_bytes,
+                 void* stream) {
+  long long L = 0;
+  int rc = grid_tokens(g, &L);
+  if (rc == WAN_OK) rc = check_shapes(B, L, H, head_dim);
+  if (rc != WAN_OK) return rc;
+  if (!q || !k || !v || !o || !tables || !workspace) return B == 0 ? WAN_OK : WAN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(tables) & 7u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return WAN_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return WAN_ERR_INVALID;
+  if (ws_bytes < wan_attn_workspace_size(WAN_OP_FWD, B, g, H, head_dim)) return WAN_ERR_INVALID;
+  if (B == 0) return WAN_OK;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != WAN_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const wan::RopeTables tab = split_tables(tables, g);
+  if (wan::launch_rope_rotate_bf16(k, workspace, B, g, H, tab, false, s) != cudaSuccess) return WAN_ERR_CUDA;
+  return wan::launch_attn_fwd(q, workspace, v, o, lse, B, (int)L, (int)L, H, g, tab, true, nullptr, scale,
+                              launch_common(*st), s);
+}
+
+int wan_xattn_fwd(const void* q, const void* k, const void* v, const int32_t* kv_lens, int Lk, void* o,
+                  float* lse, int B, wan_grid_t g, int H, int head_dim, float scale, void* stream) {
+  long long L = 0;
+  int rc = grid_tokens(g, &L);
+  if (rc == WAN_OK) rc = check_shapes(B, L, H, head_dim);
+  if (rc != WAN_OK) return rc;
+  if (Lk < 1 || Lk > 512) return WAN_ERR_INVALID;
+  if (!q || !k || !v || !o) return B == 0 ? WAN_OK : WAN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(kv_lens) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return WAN_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return WAN_ERR_INVALID;
+  if (B == 0) return WAN_OK;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != WAN_OK) return rc;
+  return wan::launch_attn_fwd(q, k, v, o, lse, B, (int)L, Lk, H, g, wan::RopeTables{}, false, kv_lens, scale,
+                              launch_common(*st), static_cast<cudaStream_t>(stream));
+}
+
+int wan_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int B, wan_grid_t g, int H, int head_dim, const float* tables,
+                 float scale, void* workspace, size_t ws_bytes, void* stream) {
+  long long L = 0;
+  int rc = grid_tokens(g, &L);
+  if (rc == WAN_OK) rc = check_shapes(B, L, H, head_dim);
+  if (rc != WAN_OK) return rc;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !tables || !workspace)
+    return B == 0 ? WAN_OK : WAN_ERR_INVALID;
+  const void* ptrs[10] = {q, k, v, o, dout, dq, dk, dv, workspace, lse};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return WAN_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(tables) & 7u) return WAN_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return WAN_ERR_INVALID;
+  if (ws_bytes < wan_attn_workspace_size(WAN_OP_BWD, B, g, H, head_dim)) return WAN_ERR_INVALID;
+  if (B == 0) return WAN_OK;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != WAN_OK) return rc;
+  return wan::launch_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, g, H, split_tables(tables, g), scale,
+                              workspace, launch_common(*st), static_cast<cudaStream_t>(stream));
+}
+
+int wan_get_device_status(void* stream) {
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != WAN_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return WAN_ERR_CUDA;
+  int v = 0;
+  const int zero = 0;
+  if (cudaMemcpy(&v, st->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return WAN_ERR_CUDA;
+  if (v != 0 && cudaMemcpy(st->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return WAN_ERR_CUDA;
+  return v == 0 ? WAN_OK : v;
+}
+
+int wan_debug_inject_stall(int count, int timeout_ms) {
+  if (count < 0 || timeout_ms < 1 || timeout_ms > 10000) return WAN_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_stall_launches = count;
+  g_stall_timeout_ns = (uint64_t)timeout_ms * 1000000ull;
+  return WAN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,414 @@
+// Attention forward for sm_103a: tcgen05 MMAs with TMEM accumulators, TMA
+// K/V tiles, online softmax.
+//
+// What is computed: for each (b, h) and query row i,
+//   O_i = sum_j softmax_j(scale * q_i . k_j) v_j,   LSE_i = log sum_j exp(scale * q_i . k_j)
+// over all keys (self-attention: full, non-causal spatio-temporal attention
+// over every latent token - "Wan Team, Alibaba (2025)" anthology note, Key
+// takeaways) or over the valid text keys (cross-attention to at most 512 umT5
+// tokens - gojay.top "Wan2.1" reading, DiT backbone and config table ⑥).
+// With 3D RoPE (same page, DiT 块) the query tile is rotated in shared memory
+// right after it lands; keys arrive already rotated.
+//
+// CTA = 2 query tiles of 128 rows of one (b, h); loop over 128-key tiles.
+//   warps 0-3  softmax of query tile 0 (one thread per row)
+//   warps 4-7  softmax of query tile 1
+//   warp  8    TMA producer (Q once, then K_j, V_j into a 4-slot ring)
+//   warp  9    MMA issuer (one thread) and TMEM owner
+// TMEM (512 columns x 128 lanes, fp32): S0 [0,128) S1 [128,256) O0 [256,384)
+// O1 [384,512). P_t (bf16, two per column) overwrites the first 64 columns of
+// S_t and is the A operand of O_t += P_t V_j straight from TMEM.
+// Per key tile the MMA order is PV0(j), QK0(j+1), PV1(j), QK1(j+1): softmax of
+// tile 0 for j+1 overlaps the tensor work of tile 1 and vice versa. Because
+// tcgen05 MMAs from one thread run in issue order, QK_t(j+1) never overwrites
+// P_t(j) before PV_t(j) has read it, and O_t is final for iteration j once
+// S_t(j+1) is signalled.
+// Softmax keeps a per-row reference max m and rescales O (in TMEM) and l only
+// when the tile max exceeds m by more than 2^8 in the exp2 domain; the final
+// O / l is exact for any reference, and p <= 256 stays well inside bf16.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace wan {
+
+namespace {
+
+constexpr int kBlockM = 128;
+constexpr int kQTiles = 2;
+constexpr int kBlockN = 128;
+constexpr int kStages = 4;
+constexpr int kTileBytes = 128 * 128 * 2;
+constexpr int kHalfBytes = kTileBytes / 2;
+constexpr int kThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kSmemBytes = (kQTiles + kStages) * kTileBytes + 1024;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct FwdArgs {
+  __nv_bfloat16* o;
+  float* lse;
+  const int32_t* kv_lens;
+  RopeTables tab;
+  int Lq, Lk, H, Hp, Wp;
+  float scale_log2;
+  LaunchCommon lc;
+};
+
+__device__ __forceinline__ void raise_abort(volatile int* abort, int* err) {
+  *abort = 1;
+  atomicCAS(err, 0, kDevTimeout);
+}
+
+// Warp-uniform bounded wait.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
+                                          uint64_t to) {
+  bool ok = mbar_wait(bar, parity, abort, to);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok && (threadIdx.x & 31) == 0) raise_abort(abort, err);
+  return ok;
+}
+
+// Rotate row r of a swizzled [128 x 128] bf16 tile in place by the 3D RoPE
+// angles of token `row`.
+__device__ __forceinline__ void rope_row_in_smem(uint8_t* tile, int r, int row, const FwdArgs& a) {
+  const int w = row % a.Wp;
+  const int tmp = row / a.Wp;
+  const int hh = tmp % a.Hp;
+  const int t = tmp / a.Hp;
+  const float2* ct = a.tab.t + t * kPairsT;
+  const float2* ch = a.tab.h + hh * kPairsH;
+  const float2* cw = a.tab.w + w * kPairsW;
+#pragma unroll 4
+  for (int c = 0; c < 16; ++c) {
+    uint4* p = reinterpret_cast<uint4*>(tile + (c >> 3) * kHalfBytes + sw128_offset(r, c & 7));
+    uint4 v = *p;
+    uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int pair = c * 4 + k;
+      const float2 cs = pair < kPairsT ? ct[pair] : (pair < kPairsT + kPairsH ? ch[pair - kPairsT]
+                                                                                : cw[pair - kPairsT - kPairsH]);
+      const float x0 = __uint_as_float(wd[k] << 16);
+      const float x1 = __uint_as_float(wd[k] & 0xFFFF0000u);
+      wd[k] = pack_bf16x2(x0 * cs.x - x1 * cs.y, x0 * cs.y + x1 * cs.x);
+    }
+    *p = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+  }
+}
+
+template <bool kRope>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + kQTiles * kTileBytes;
+
+  __shared__ __align__(8) uint64_t bar_q_full[kQTiles], bar_q_ready[kQTiles];
+  __shared__ __align__(8) uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
+  __shared__ __align__(8) uint64_t bar_s_full[kQTiles], bar_p_full[kQTiles], bar_o_full[kQTiles];
+  __shared__ __align__(8) uint64_t bar_drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int q0 = blockIdx.x * (kBlockM * kQTiles);
+  const uint64_t to = a.lc.timeout_ns;
+  volatile int* abort = &abort_sh;
+
+  int n_valid = a.Lk;
+  if (a.kv_lens != nullptr) {
+    const int v = a.kv_lens[b];
+    n_valid = v < 0 ? 0 : (v > a.Lk ? a.Lk : v);
+  }
+  const int n_tiles = (n_valid + kBlockN - 1) / kBlockN;
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(&bar_q_full[t], 1);
+      mbar_init(&bar_q_ready[t], 4);
+      mbar_init(&bar_s_full[t], 1);
+      mbar_init(&bar_p_full[t], 4);
+      mbar_init(&bar_o_full[t], 1);
+    }
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar_kv_full[s], 1);
+      mbar_init(&bar_kv_empty[s], 1);
+    }
+    mbar_init(&bar_drain, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&tmem_base_sh, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      for (int t = 0; t < kQTiles; ++t) {
+        mbar_arrive_expect_tx(&bar_q_full[t], kTileBytes);
+        tma_load_4d(sQ + t * kTileBytes, &tm_q, &bar_q_full[t], 0, h, q0 + t * kBlockM, b);
+        tma_load_4d(sQ + t * kTileBytes + kHalfBytes, &tm_q, &bar_q_full[t], 64, h, q0 + t * kBlockM, b);
+      }
+      int issued[kStages];
+      for (int s = 0; s < kStages; ++s) issued[s] = 0;
+      for (int i = 0; i < 2 * n_tiles; ++i) {
+        const int slot = i % kStages;
+        const int use = i / kStages;
+        if (use > 0 && !mbar_wait(&bar_kv_empty[slot], (use - 1) & 1, abort, to)) {
+          raise_abort(abort, a.lc.err);
+          break;
+        }
+        if (a.lc.stall && i == 1) continue;  // test hook: V_0 never arrives
+        const CUtensorMap* m = (i & 1) ? &tm_v : &tm_k;
+        const int row = (i >> 1) * kBlockN;
+        uint8_t* dst = sKV + slot * kTileBytes;
+        mbar_arrive_expect_tx(&bar_kv_full[slot], kTileBytes);
+        tma_load_4d(dst, m, &bar_kv_full[slot], 0, h, row, b);
+        tma_load_4d(dst + kHalfBytes, m, &bar_kv_full[slot], 64, h, row, b);
+        issued[slot] = use + 1;
+      }
+      if (*abort) {
+        // Let every copy still in flight land before shared memory is released.
+        for (int s = 0; s < kStages; ++s)
+          if (issued[s] > 0) mbar_wait(&bar_kv_full[s], (issued[s] - 1) & 1, nullptr, to);
+        for (int t = 0; t < kQTiles; ++t) mbar_wait(&bar_q_full[t], 0, nullptr, to);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // Q (K-major) x K (K-major)
+      const uint32_t idesc_o = idesc_bf16_f32(128, 128, 0, 1);  // P (TMEM) x V (MN-major)
+      const uint32_t sq = smem_u32(sQ);
+      const uint32_t skv = smem_u32(sKV);
+      auto issue_qk = [&](int t, int slot) {
+        const uint32_t qa = sq + t * kTileBytes;
+        const uint32_t ka = skv + slot * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          umma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_s,
+                  kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int slot, bool acc) {
+        const uint32_t va = skv + slot * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, sdesc_sw128(va + kk * 2048, kHalfBytes, 1024),
+                  idesc_o, (acc || kk > 0) ? 1u : 0u);
+      };
+      bool ok = true;
+      for (int t = 0; t < kQTiles && ok; ++t) ok = mbar_wait(&bar_q_ready[t], 0, abort, to);
+      if (ok && n_tiles > 0) {
+        ok = mbar_wait(&bar_kv_full[0], 0, abort, to);
+        if (ok) {
+          tc_fence_after();
+          issue_qk(0, 0);
+          umma_commit(&bar_s_full[0]);
+          issue_qk(1, 0);
+          umma_commit(&bar_s_full[1]);
+          umma_commit(&bar_kv_empty[0]);
+        }
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const int iv = 2 * j + 1;
+          const int vslot = iv % kStages;
+          ok = mbar_wait(&bar_kv_full[vslot], (iv / kStages) & 1, abort, to);
+          const bool has_next = j + 1 < n_tiles;
+          const int ik = 2 * j + 2;
+          const int kslot = ik % kStages;
+          if (ok && has_next) ok = mbar_wait(&bar_kv_full[kslot], (ik / kStages) & 1, abort, to);
+          for (int t = 0; t < kQTiles && ok; ++t) {
+            ok = mbar_wait(&bar_p_full[t], j & 1, abort, to);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, vslot, j > 0);
+            if (t == kQTiles - 1) umma_commit(&bar_kv_empty[vslot]);
+            if (!has_next) {
+              umma_commit(&bar_o_full[t]);
+            } else {
+              issue_qk(t, kslot);
+              umma_commit(&bar_s_full[t]);
+              if (t == kQTiles - 1) umma_commit(&bar_kv_empty[kslot]);
+            }
+          }
+        }
+      }
+      if (!ok) raise_abort(abort, a.lc.err);
+      // Every MMA of this CTA must be done before TMEM is released.
+      umma_commit(&bar_drain);
+      mbar_wait(&bar_drain, 0, nullptr, to);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int row = q0 + t * kBlockM + r;
+    const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + t * 128;
+    const uint32_t tO = tmem + lane_addr + 256 + t * 128;
+    const float sl2 = a.scale_log2;
+
+    bool ok = warp_wait(&bar_q_full[t], 0, abort, a.lc.err, to);
+    if (kRope && ok && row < a.Lq) rope_row_in_smem(sQ + t * kTileBytes, r, row, a);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar_q_ready[t]);
+
+    float m_ref = -INFINITY;
+    float l = 0.f;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      ok = warp_wait(&bar_s_full[t], j & 1, abort, a.lc.err, to);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+      tmem_ld_wait();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
+      const int valid = n_valid - j * kBlockN;
+      if (valid < kBlockN) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= valid) s[i] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+      const float m_new = fmaxf(m_ref, mx);
+      if (j == 0) {
+        m_ref = m_new;
+      } else {
+        const bool need = (m_new - m_ref) * sl2 > kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2_approx((m_ref - m_new) * sl2) : 1.0f;
+          if (need) {
+            l *= alpha;
+            m_ref = m_new;
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + c * 32, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(tO + c * 32, ov);
+          }
+        }
+      }
+      const float neg = -m_ref * sl2;
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, neg));
+          const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, neg));
+          lsum += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + c * 16, pk);
+      }
+      l += lsum;
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p_full[t]);
+    }
+
+    // ------------------------------------------------------------ epilogue
+    __nv_bfloat16* orow = a.o + ((static_cast<size_t>(b) * a.Lq + row) * a.H + h) * kHeadDim;
+    if (n_tiles == 0) {
+      if (row < a.Lq) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+        for (int c = 0; c < 16; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+        if (a.lse) a.lse[(static_cast<size_t>(b) * a.H + h) * a.Lq + row] = -INFINITY;
+      }
+    } else if (ok) {
+      ok = warp_wait(&bar_o_full[t], 0, abort, a.lc.err, to);
+      if (ok) {
+        tc_fence_after();
+        const float inv = 1.0f / l;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tO + c * 32, ov);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
+          if (row < a.Lq) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+        if (a.lse && row < a.Lq)
+          a.lse[(static_cast<size_t>(b) * a.H + h) * a.Lq + row] = (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+int launch_attn_fwd(const void* q, const void* k_rot, const void* v, void* o, float* lse, int B, int Lq, int Lk,
+                    int H, wan_grid_t g, RopeTables tab, bool rope, const int32_t* kv_lens, float scale,
+                    const LaunchCommon& lc, cudaStream_t s) {
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_bld(&tq, q, B, Lq, H, kHeadDim, 128)) return WAN_ERR_CUDA;
+  if (!make_tmap_bld(&tk, k_rot, B, Lk, H, kHeadDim, 128)) return WAN_ERR_CUDA;
+  if (!make_tmap_bld(&tv, v, B, Lk, H, kHeadDim, 128)) return WAN_ERR_CUDA;
+  FwdArgs a;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.kv_lens = kv_lens;
+  a.tab = tab;
+  a.Lq = Lq;
+  a.Lk = Lk;
+  a.H = H;
+  a.Hp = g.Hp;
+  a.Wp = g.Wp;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.lc = lc;
+  dim3 grid((Lq + kBlockM * kQTiles - 1) / (kBlockM * kQTiles), H, B);
+  auto kern = rope ? attn_fwd_kernel<true> : attn_fwd_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+    return WAN_ERR_CUDA;
+  kern<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, a);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+}  // namespace wan

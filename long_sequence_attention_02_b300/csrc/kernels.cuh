@@ -1,0 +1,46 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "wan_attn.h"
+
+namespace wan {
+
+constexpr int kHeadDim = 128;
+constexpr int kPairsT = 22;  // rotary pairs of the t band at head_dim 128 (44 dims)
+constexpr int kPairsH = 21;  // h band (42 dims)
+constexpr int kPairsW = 21;  // w band (42 dims)
+
+// Device pointers to the three per-axis float2 {cos, sin} tables.
+struct RopeTables {
+  const float2* t;  // [F][kPairsT]
+  const float2* h;  // [Hp][kPairsH]
+  const float2* w;  // [Wp][kPairsW]
+};
+
+struct LaunchCommon {
+  int* err;             // device error word
+  uint64_t timeout_ns;  // bound of every device-side wait
+  int stall;            // test hook: producer withholds one tile
+};
+
+// y = R(pos) x (or R(pos)^T x when inverse) for bf16 [B, L, H, 128]; y may equal x.
+cudaError_t launch_rope_rotate_bf16(const void* x, void* y, int B, wan_grid_t g, int H, RopeTables tab,
+                                    bool inverse, cudaStream_t s);
+
+// Forward attention. With rope = true (self-attention) q is rotated inside the
+// kernel and k_rot must already be rotated; with rope = false it is plain
+// cross-attention over Lk keys with optional per-batch valid lengths.
+int launch_attn_fwd(const void* q, const void* k_rot, const void* v, void* o, float* lse, int B, int Lq, int Lk,
+                    int H, wan_grid_t g, RopeTables tab, bool rope, const int32_t* kv_lens, float scale,
+                    const LaunchCommon& lc, cudaStream_t s);
+
+// Backward. Workspace layout is defined in attn_bwd.cu.
+size_t attn_bwd_workspace_bytes(int B, int L, int H);
+int launch_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                    void* dq, void* dk, void* dv, int B, wan_grid_t g, int H, RopeTables tab, float scale,
+                    void* workspace, const LaunchCommon& lc, cudaStream_t s);
+
+}  // namespace wan

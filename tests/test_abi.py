@@ -1,0 +1,133 @@
+"""The C-ABI library: it loads, exports what the header declares, and rejects
+bad arguments on the host before touching CUDA (no GPU needed)."""
+import os
+import re
+
+import pytest
+
+import long_sequence_attention_02_b300 as wan
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wan_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from long_sequence_attention_02_b300 import build
+
+    build.build_attn()
+    return wan.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(wan_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_functions() == sorted(wan.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert wan.status_str(0) == "WAN_OK"
+    for code in (1, 2, 3, 4):
+        assert wan.status_str(code).startswith("WAN_ERR")
+    assert wan.wan_version() >= 100
+
+
+def test_table_and_workspace_sizes(lib):
+    assert wan.wan_rope3d_tables_size((3, 8, 8)) == (3 * 22 + 8 * 21 + 8 * 21) * 8
+    assert wan.wan_rope3d_tables_size((21, 45, 80)) == (21 * 22 + 45 * 21 + 80 * 21) * 8
+    assert wan.wan_rope3d_tables_size((0, 8, 8)) == 0
+    assert wan.wan_rope3d_tables_size((3, 8, 8), 64) == 0
+    n = 1 * 75600 * 40 * 128 * 2
+    assert wan.wan_attn_workspace_size(wan.WAN_OP_FWD, 1, (21, 45, 80), 40) >= n
+    assert wan.wan_attn_workspace_size(wan.WAN_OP_BWD, 1, (4, 4, 4), 2) > 0
+    assert wan.wan_attn_workspace_size(7, 1, (4, 4, 4), 2) == 0
+
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced: every case fails validation first
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    g = (2, 4, 4)
+    ws = wan.wan_attn_workspace_size(wan.WAN_OP_FWD, 1, g, 2)
+    ok = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, grid=g, H=2, head_dim=128, tables=FAKE,
+              scale=0.088, workspace=FAKE, ws_bytes=ws, stream=0)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return wan.wan_attn_fwd(**a)
+
+    assert call(q=None) == wan.WAN_ERR_INVALID
+    assert call(tables=None) == wan.WAN_ERR_INVALID
+    assert call(workspace=None) == wan.WAN_ERR_INVALID
+    assert call(q=FAKE + 8) == wan.WAN_ERR_INVALID
+    assert call(o=FAKE + 2) == wan.WAN_ERR_INVALID
+    assert call(ws_bytes=ws - 1) == wan.WAN_ERR_INVALID
+    assert call(grid=(0, 4, 4)) == wan.WAN_ERR_INVALID
+    assert call(grid=(2, -1, 4)) == wan.WAN_ERR_INVALID
+    assert call(H=0) == wan.WAN_ERR_INVALID
+    assert call(B=-1) == wan.WAN_ERR_INVALID
+    assert call(scale=0.0) == wan.WAN_ERR_INVALID
+    assert call(scale=float("nan")) == wan.WAN_ERR_INVALID
+    assert call(head_dim=64) == wan.WAN_ERR_UNSUPPORTED
+    # zero work is a no-op that launches nothing
+    assert call(B=0, q=None, k=None, v=None, o=None, lse=None, workspace=None, ws_bytes=0) == wan.WAN_OK
+
+
+def test_xattn_rejects_bad_arguments(lib):
+    g = (2, 4, 4)
+    ok = dict(q=FAKE, k=FAKE, v=FAKE, kv_lens=None, Lk=77, o=FAKE, lse=None, B=2, grid=g, H=2, head_dim=128,
+              scale=0.088, stream=0)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return wan.wan_xattn_fwd(**a)
+
+    assert call(Lk=0) == wan.WAN_ERR_INVALID
+    assert call(Lk=513) == wan.WAN_ERR_INVALID
+    assert call(k=None) == wan.WAN_ERR_INVALID
+    assert call(kv_lens=FAKE + 2) == wan.WAN_ERR_INVALID
+    assert call(lse=FAKE + 1) == wan.WAN_ERR_INVALID
+    assert call(head_dim=96) == wan.WAN_ERR_UNSUPPORTED
+    assert call(B=0, q=None) == wan.WAN_OK
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    g = (2, 4, 4)
+    ws = wan.wan_attn_workspace_size(wan.WAN_OP_BWD, 1, g, 2)
+    ok = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, dout=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=1, grid=g, H=2,
+              head_dim=128, tables=FAKE, scale=0.088, workspace=FAKE, ws_bytes=ws, stream=0)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return wan.wan_attn_bwd(**a)
+
+    for name in ("q", "k", "v", "o", "lse", "dout", "dq", "dk", "dv", "tables", "workspace"):
+        assert call(**{name: None}) == wan.WAN_ERR_INVALID, name
+    assert call(dq=FAKE + 4) == wan.WAN_ERR_INVALID
+    assert call(ws_bytes=ws - 16) == wan.WAN_ERR_INVALID
+    assert call(head_dim=256) == wan.WAN_ERR_UNSUPPORTED
+
+
+def test_tables_reject_bad_arguments(lib):
+    assert wan.wan_rope3d_tables((3, 8, 8), 128, 10000.0, None, 0) == wan.WAN_ERR_INVALID
+    assert wan.wan_rope3d_tables((3, 8, 8), 128, 0.5, FAKE, 0) == wan.WAN_ERR_INVALID
+    assert wan.wan_rope3d_tables((3, 0, 8), 128, 1e4, FAKE, 0) == wan.WAN_ERR_INVALID
+    assert wan.wan_rope3d_tables((3, 8, 8), 100, 1e4, FAKE, 0) == wan.WAN_ERR_UNSUPPORTED
+
+
+def test_debug_hook_argument_checks(lib):
+    assert wan.wan_debug_inject_stall(-1, 10) == wan.WAN_ERR_INVALID
+    assert wan.wan_debug_inject_stall(1, 0) == wan.WAN_ERR_INVALID
+    assert wan.wan_debug_inject_stall(0, 100) == wan.WAN_OK

@@ -1,0 +1,56 @@
+"""Failure detection without a GPU fault: a producer that withholds one tile
+makes the consumers' bounded waits expire; the kernel reports WAN_ERR_TIMEOUT
+through the device error word, frees its resources and returns, and the
+context stays usable."""
+import math
+
+import numpy as np
+import pytest
+
+import long_sequence_attention_02_b300 as wan
+from long_sequence_attention_02_b300 import synth
+from oracle import ref
+from tests._util import bits, compare, dev_to_f64, f64, to_dev
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+def _tiny():
+    grid, B, H = (2, 4, 8), 1, 1
+    shape = (B, 64, H, 128)
+    return grid, [bits(7, s, shape) for s in (synth.STREAM_Q, synth.STREAM_K, synth.STREAM_V)]
+
+
+def test_withheld_tile_times_out_and_context_survives():
+    grid, (qb, kb, vb) = _tiny()
+    q, k, v = to_dev(qb), to_dev(kb), to_dev(vb)
+    assert wan.wan_get_device_status() == wan.WAN_OK
+    wan.check(wan.wan_debug_inject_stall(1, 200))
+    try:
+        o, lse = wan.attention_forward(q, k, v, grid)  # launch itself succeeds
+    finally:
+        wan.wan_debug_inject_stall(0, 100)
+    assert wan.wan_get_device_status() == wan.WAN_ERR_TIMEOUT
+    assert wan.wan_get_device_status() == wan.WAN_OK  # the word was cleared
+    # the next launch is normal and correct
+    o, lse = wan.attention_forward(q, k, v, grid)
+    assert wan.wan_get_device_status() == wan.WAN_OK
+    o_ref, lse_ref = ref.self_attention_fwd(f64(qb), f64(kb), f64(vb), grid)
+    compare(dev_to_f64(o), o_ref, "O after recovery")
+    compare(dev_to_f64(lse), lse_ref, "LSE after recovery")
+
+
+def test_timeout_in_cross_attention():
+    grid, (qb, kb, vb) = _tiny()
+    q, k, v = to_dev(qb), to_dev(kb), to_dev(vb)
+    wan.check(wan.wan_debug_inject_stall(1, 100))
+    try:
+        wan.cross_attention_forward(q, k, v, None, grid)
+    finally:
+        wan.wan_debug_inject_stall(0, 100)
+    assert wan.wan_get_device_status() == wan.WAN_ERR_TIMEOUT
+    o, _ = wan.cross_attention_forward(q, k, v, None, grid)
+    assert wan.wan_get_device_status() == wan.WAN_OK
+    o_ref, _ = ref.cross_attention_fwd(f64(qb), f64(kb), f64(vb), [64])
+    compare(dev_to_f64(o), o_ref, "xattn O after recovery")
