@@ -1,0 +1,502 @@
+"""Benchmark of the B300 attention hot path (prints ONE JSON line on rank 0).
+
+Headline workload: 14B-shaped 720p self-attention forward with 3D RoPE,
+B = 1, grid 21x45x80 = 75,600 tokens, H = 40, d = 128, bf16 N(0,1) inputs.
+A step is one wan_attn_fwd call (K RoPE pre-pass + attention kernel) on
+inputs already resident in HBM; the RoPE tables are a per-grid constant built
+once before timing. value = 4*B*H*L^2*d / step time (TFLOP/s).
+
+Also reported (same run): the 480p 1.3B self-attention forward, the
+cross-attention forward and the 64^3 training step (forward + backward).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs its own independent copy of the workload
+(weak scaling; the path has no data exchange between ranks), and the step
+time is the max over ranks. `--impl reference` times the fp64 CPU oracle on
+a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, HERE)
+
+METRIC = "attention TFLOP/s (bf16 fwd/bwd) at 32,760 and 75,600 tokens; % of dense BF16 peak"
+L2_BYTES = 126 * 2 ** 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(HERE, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p["bf16_tflops_sustained"], "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (timing only: barrier and max over ranks)
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = os.environ.get("WAN_BENCH_BACKEND", "nccl")
+        if backend == "nccl":
+            import torch
+
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: units all ranks processed / slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import long_sequence_attention_02_b300 as wan
+    from long_sequence_attention_02_b300.workloads import WORKLOADS
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = _peaks()
+    w = WORKLOADS[args.workload]
+    B, L, H, d, grid = w.B, w.L, w.H, w.d, w.grid
+    flops = 4.0 * B * H * L * L * d
+    scale = 1.0 / math.sqrt(d)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + rank)
+    q = torch.randn(B, L, H, d, device=dev, generator=gen).bfloat16()
+    k = torch.randn(B, L, H, d, device=dev, generator=gen).bfloat16()
+    v = torch.randn(B, L, H, d, device=dev, generator=gen).bfloat16()
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, L, device=dev)
+    tables = wan.rope_tables(grid, device=dev)
+    ws_bytes = wan.wan_attn_workspace_size(wan.WAN_OP_FWD, B, grid, H, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    in_bytes = 3 * q.numel() * 2
+
+    def step(prof=None):
+        if prof is not None:
+            wan.check(wan.wan_profile_set_events(*prof))
+        wan.check(wan.wan_attn_fwd(q, k, v, o, lse, B, grid, H, d, tables, scale, ws, ws_bytes, stream))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    wan.check(wan.wan_get_device_status())
+
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(kev[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(world)
+    wan.check(wan.wan_get_device_status())
+    ms = e0.elapsed_time(e1) / args.steps
+    kernel_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
+    ms_max = max_over_ranks(ms, world)
+    value = aggregate(flops, world, ms_max / 1e3) / 1e12
+    kernel_tflops = flops / (kernel_ms / 1e3) / 1e12
+
+    # ----- end to end through the C ABI with host buffers
+    qh = q.cpu().pin_memory()
+    kh = k.cpu().pin_memory()
+    vh = v.cpu().pin_memory()
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lseh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        wan.check(wan.wan_attn_fwd(q, k, v, o, lse, B, grid, H, d, tables, scale, ws, ws_bytes, stream))
+        oh.copy_(o, non_blocking=True)
+        lseh.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 5))
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1) / e2e_steps, world)
+    e2e = {"value": round(aggregate(flops, world, e2e_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
+           "ms_per_step": round(e2e_ms, 3)}
+    del qh, kh, vh, oh, lseh
+
+    also = {}
+    if not args.no_extras and rank == 0:
+        also = extras(wan, torch, dev, peaks)
+
+    peak = peaks["bf16_tflops_sustained"]
+    traffic = None
+    prof_path = os.path.join(HERE, "profiles", "traffic.json")
+    if os.path.exists(prof_path):
+        try:
+            with open(prof_path) as f:
+                tr = json.load(f)
+            ent = tr.get("attn_fwd_kernel", {})
+            if ent.get("source_fingerprint") == source_fingerprint():
+                traffic = ent.get("bytes_per_launch")
+        except Exception:
+            traffic = None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: bf16 N(0,1) Q, K, V (torch generator, seed 1000+rank)",
+        "config": {"workload": w.name, "B": B, "grid": list(grid), "tokens": L, "heads": H, "head_dim": d,
+                   "theta": 10000.0, "flop_per_step": flops,
+                   "l2": f"inputs {in_bytes / 2**30:.2f} GiB > L2 126 MB (no flush needed)",
+                   "frac_of_2.25PF_spec": round(value / 2250.0, 4)},
+        "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": round(kernel_tflops, 2),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(kernel_tflops / peak, 4),
+                     "peak_kind": f"bf16 sustained ({peaks['source']})",
+                     "frac_of_burst": round(kernel_tflops / peaks["bf16_tflops"], 4),
+                     "kernel_ms": round(kernel_ms, 3), "traffic": traffic},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+    }
+    if also:
+        line["also"] = also
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_rows)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def extras(wan, torch, dev, peaks):
+    """Secondary workloads, each timed with CUDA events (3 iterations after 2 warm-ups)."""
+    from long_sequence_attention_02_b300.workloads import WORKLOADS
+
+    out = {}
+    stream = torch.cuda.current_stream(dev)
+
+    def timeit(fn, iters=3, warm=2, prof=False):
+        for _ in range(warm):
+            fn(None)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(iters):
+            fn(ev[i] if prof else None)
+        b.record(stream)
+        torch.cuda.synchronize()
+        wan.check(wan.wan_get_device_status())
+        tot = a.elapsed_time(b) / iters
+        ker = sum(x.elapsed_time(y) for x, y in ev) / iters if prof else None
+        return tot, ker
+
+    # 480p self-attention forward
+    w = WORKLOADS["wan1.3b_480p_self_fwd"]
+    B, L, H, d = w.B, w.L, w.H, w.d
+    q = torch.randn(B, L, H, d, device=dev).bfloat16()
+    k, v = torch.randn_like(q), torch.randn_like(q)
+    o, lse = torch.empty_like(q), torch.empty(B, H, L, device=dev)
+    tab = wan.rope_tables(w.grid, device=dev)
+    wsb = wan.wan_attn_workspace_size(0, B, w.grid, H, d)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+
+    def f480(p):
+        if p is not None:
+            wan.wan_profile_set_events(*p)
+        wan.check(wan.wan_attn_fwd(q, k, v, o, lse, B, w.grid, H, d, tab, 1 / math.sqrt(d), ws, wsb, stream))
+
+    tot, ker = timeit(f480, iters=10, prof=True)
+    fl = 4.0 * B * H * L * L * d
+    out[w.name] = {"ms": round(tot, 3), "tflops": round(fl / tot / 1e9, 1), "kernel_tflops": round(fl / ker / 1e9, 1)}
+    del q, k, v, o, lse, ws
+
+    # cross-attention forward
+    w = WORKLOADS["wan14b_720p_cross_fwd"]
+    B, Lq, H, d, Lk = w.B, w.L, w.H, w.d, w.Lk
+    q = torch.randn(B, Lq, H, d, device=dev).bfloat16()
+    k = torch.randn(B, Lk, H, d, device=dev).bfloat16()
+    v = torch.randn_like(k)
+    from long_sequence_attention_02_b300 import synth
+
+    lens_np = synth.kv_lens(0, B)
+    lens = torch.from_numpy(lens_np).to(dev)
+    o, lse = torch.empty_like(q), torch.empty(B, H, Lq, device=dev)
+
+    def fx(p):
+        if p is not None:
+            wan.wan_profile_set_events(*p)
+        wan.check(wan.wan_xattn_fwd(q, k, v, lens, Lk, o, lse, B, w.grid, H, d, 1 / math.sqrt(d), stream))
+
+    tot, _ = timeit(fx, iters=10)
+    nominal = 4.0 * B * H * Lq * Lk * d
+    useful = 4.0 * H * Lq * d * float(lens_np.sum())
+    hbm = (q.numel() * 2 * 2 + lse.numel() * 4 + k.numel() * 2 * 2)
+    out[w.name] = {"ms": round(tot, 3), "tflops_nominal": round(nominal / tot / 1e9, 1),
+                   "tflops_useful": round(useful / tot / 1e9, 1), "kv_lens": lens_np.tolist(),
+                   "gbs": round(hbm / tot / 1e6, 1), "hbm_frac": round(hbm / tot / 1e6 / peaks["hbm_gbs"], 3)}
+    del q, k, v, o, lse
+
+    # training step: forward + backward at 64^3 tokens
+    w = WORKLOADS["train_64x64x64_fwd_bwd"]
+    B, L, H, d = w.B, w.L, w.H, w.d
+    q = torch.randn(B, L, H, d, device=dev).bfloat16()
+    k, v, do = torch.randn_like(q), torch.randn_like(q), torch.randn_like(q)
+    o, lse = torch.empty_like(q), torch.empty(B, H, L, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    tab = wan.rope_tables(w.grid, device=dev)
+    wsf = wan.wan_attn_workspace_size(0, B, w.grid, H, d)
+    wsb = wan.wan_attn_workspace_size(1, B, w.grid, H, d)
+    ws = torch.empty(max(wsf, wsb), dtype=torch.uint8, device=dev)
+    sc = 1 / math.sqrt(d)
+
+    def ftrain(p):
+        wan.check(wan.wan_attn_fwd(q, k, v, o, lse, B, w.grid, H, d, tab, sc, ws, wsf, stream))
+        if p is not None:
+            wan.wan_profile_set_events(*p)
+        wan.check(wan.wan_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, w.grid, H, d, tab, sc, ws, wsb, stream))
+
+    def ffwd(p):
+        if p is not None:
+            wan.wan_profile_set_events(*p)
+        wan.check(wan.wan_attn_fwd(q, k, v, o, lse, B, w.grid, H, d, tab, sc, ws, wsf, stream))
+
+    ffl = 4.0 * B * H * L * L * d
+    tot_f, ker_f = timeit(ffwd, iters=2, warm=1, prof=True)
+    tot, ker_b = timeit(ftrain, iters=2, warm=1, prof=True)
+    out[w.name] = {"ms_fwd": round(tot_f, 2), "ms_fwd_bwd": round(tot, 2),
+                   "tflops_fwd": round(ffl / tot_f / 1e9, 1),
+                   "tflops_bwd_kernel": round(2.5 * ffl / ker_b / 1e9, 1),
+                   "tflops_bwd": round(2.5 * ffl / (tot - tot_f) / 1e9, 1),
+                   "tflops_step": round(3.5 * ffl / tot / 1e9, 1)}
+    return out
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+
+
+def source_fingerprint() -> str:
+    import hashlib
+
+    h = hashlib.sha1()
+    for name in ("attn_fwd.cu", "common.cuh"):
+        with open(os.path.join(HERE, "long_sequence_attention_02_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def _oracle_rows(w, rows_per_head: int, heads: int, seed: int = 0):
+    """Time the oracle on `rows_per_head` query rows of `heads` heads."""
+    import numpy as np
+
+    from long_sequence_attention_02_b300 import synth
+    from oracle import ref
+
+    L, d = w.L, w.d
+    H = w.H
+    t0 = time.perf_counter()
+    n = 0
+    for h in range(heads):
+        idx_k = (np.arange(L, dtype=np.uint64)[:, None] * H + h) * d + np.arange(d, dtype=np.uint64)[None, :]
+        kh = synth.bf16_bits_to_f64(synth.normal_bf16_at(seed, synth.STREAM_K, idx_k))
+        vh = synth.bf16_bits_to_f64(synth.normal_bf16_at(seed, synth.STREAM_V, idx_k))
+        rows = np.arange(rows_per_head, dtype=np.int64) * (L // rows_per_head)
+        idx_q = (rows.astype(np.uint64)[:, None] * H + h) * d + np.arange(d, dtype=np.uint64)[None, :]
+        qr = synth.bf16_bits_to_f64(synth.normal_bf16_at(seed, synth.STREAM_Q, idx_q))
+        ref.self_attention_fwd_rows(qr, rows, kh, vh, w.grid)
+        n += rows_per_head
+    dt = time.perf_counter() - t0
+    return n, dt
+
+
+def cpu_baseline(w, rows_per_head: int):
+    n, dt = _oracle_rows(w, rows_per_head, heads=2)
+    fl = 4.0 * w.L * w.d * n
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} query rows (2 heads x {rows_per_head}) of {w.name} against all {w.L} keys, "
+                      f"fp64 numpy, {dt:.1f} s", "rows_per_s": round(n / dt, 1)}
+
+
+def run_reference(args, rank, world):
+    from long_sequence_attention_02_b300.workloads import WORKLOADS
+
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        _oracle_rows(w, rows, heads=1)
+    times, n_tot = [], 0
+    for _ in range(args.steps):
+        n, dt = _oracle_rows(w, rows, heads=1)
+        times.append(dt)
+        n_tot += n
+    dt = sum(times)
+    fl = 4.0 * w.L * w.d * n_tot
+    value = fl / dt / 1e12
+    sample = f"{rows} query rows of one head per step against all {w.L} keys (fp64 numpy oracle)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: bf16 N(0,1) from the seeded SplitMix64 generator",
+        "config": {"workload": w.name, "B": w.B, "grid": list(w.grid), "tokens": w.L, "heads": w.H,
+                   "head_dim": w.d},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="wan14b_720p_self_fwd")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--ref-rows", type=int, default=64)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -144,6 +144,16 @@ int wan_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
 int wan_get_device_status(void* stream);
 
 /*
+ * Profiling hook: when `start` and `stop` (cudaEvent_t passed as void*) are
+ * non-NULL, the next attention entry point records `start` on its stream
+ * immediately before its main attention kernel and `stop` immediately after
+ * it, so that cudaEventElapsedTime isolates that kernel from the pre- and
+ * post-passes. The hook applies to one call and then clears itself; pass
+ * NULL, NULL to clear it explicitly. The events stay owned by the caller.
+ */
+int wan_profile_set_events(void* start, void* stop);
+
+/*
  * Test hook (not for production use): make the next `count` attention kernel
  * launches on this device skip one producer arrival so that their consumers'
  * bounded waits expire after `timeout_ms`, exercising the timeout path without

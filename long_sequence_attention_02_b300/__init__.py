@@ -32,7 +32,7 @@ DEFAULT_THETA = 10000.0
 EXPORTED = (
     "wan_status_str", "wan_version", "wan_rope3d_tables_size", "wan_rope3d_tables",
     "wan_attn_workspace_size", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
-    "wan_get_device_status", "wan_debug_inject_stall",
+    "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall",
 )
 
 
@@ -70,8 +70,9 @@ def load_library(path: str = LIB_PATH):
                                  vp]
     lib.wan_get_device_status.argtypes = [vp]
     lib.wan_debug_inject_stall.argtypes = [i32, i32]
+    lib.wan_profile_set_events.argtypes = [vp, vp]
     for name in ("wan_rope3d_tables", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
-                 "wan_get_device_status", "wan_debug_inject_stall"):
+                 "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -152,6 +153,12 @@ def wan_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, grid, H, head_dim, tables
 
 def wan_get_device_status(stream=None) -> int:
     return load_library().wan_get_device_status(_stream(stream))
+
+
+def wan_profile_set_events(start, stop) -> int:
+    """start/stop: torch.cuda.Event (created with enable_timing) or None."""
+    return load_library().wan_profile_set_events(None if start is None else start.cuda_event,
+                                                 None if stop is None else stop.cuda_event)
 
 
 def wan_debug_inject_stall(count: int, timeout_ms: int) -> int:

@@ -29,6 +29,8 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 int g_stall_launches = 0;
 uint64_t g_stall_timeout_ns = 0;
+cudaEvent_t g_prof_start = nullptr;
+cudaEvent_t g_prof_stop = nullptr;
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -78,6 +80,9 @@ wan::LaunchCommon launch_common(const DeviceState& st) {
   lc.timeout_ns = kDefaultTimeoutNs;
   lc.stall = 0;
   std::lock_guard<std::mutex> lk(g_mu);
+  lc.ev_start = g_prof_start;
+  lc.ev_stop = g_prof_stop;
+  g_prof_start = g_prof_stop = nullptr;
   if (g_stall_launches > 0) {
     --g_stall_launches;
     lc.stall = 1;
@@ -230,6 +235,14 @@ int wan_get_device_status(void* stream) {
   if (v != 0 && cudaMemcpy(st->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
     return WAN_ERR_CUDA;
   return v == 0 ? WAN_OK : v;
+}
+
+int wan_profile_set_events(void* start, void* stop) {
+  if ((start == nullptr) != (stop == nullptr)) return WAN_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_prof_start = static_cast<cudaEvent_t>(start);
+  g_prof_stop = static_cast<cudaEvent_t>(stop);
+  return WAN_OK;
 }
 
 int wan_debug_inject_stall(int count, int timeout_ms) {

@@ -407,7 +407,9 @@ int launch_attn_fwd(const void* q, const void* k_rot, const void* v, void* o, fl
   auto kern = rope ? attn_fwd_kernel<true> : attn_fwd_kernel<false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return WAN_ERR_CUDA;
+  record_start(lc, s);
   kern<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, a);
+  record_stop(lc, s);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
 

@@ -24,11 +24,24 @@ struct LaunchCommon {
   int* err;             // device error word
   uint64_t timeout_ns;  // bound of every device-side wait
   int stall;            // test hook: producer withholds one tile
+  cudaEvent_t ev_start; // profiling hook: recorded around the main kernel (may be null)
+  cudaEvent_t ev_stop;
 };
+
+inline void record_start(const LaunchCommon& lc, cudaStream_t s) {
+  if (lc.ev_start) cudaEventRecord(lc.ev_start, s);
+}
+inline void record_stop(const LaunchCommon& lc, cudaStream_t s) {
+  if (lc.ev_stop) cudaEventRecord(lc.ev_stop, s);
+}
 
 // y = R(pos) x (or R(pos)^T x when inverse) for bf16 [B, L, H, 128]; y may equal x.
 cudaError_t launch_rope_rotate_bf16(const void* x, void* y, int B, wan_grid_t g, int H, RopeTables tab,
                                     bool inverse, cudaStream_t s);
+
+// y(bf16) = R(pos)^T x(fp32) for [B, L, H, 128]; used for dQ.
+cudaError_t launch_rope_unrotate_f32(const float* x, void* y, int B, wan_grid_t g, int H, RopeTables tab,
+                                     cudaStream_t s);
 
 // Forward attention. With rope = true (self-attention) q is rotated inside the
 // kernel and k_rot must already be rotated; with rope = false it is plain

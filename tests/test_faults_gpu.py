@@ -54,3 +54,24 @@ def test_timeout_in_cross_attention():
     assert wan.wan_get_device_status() == wan.WAN_OK
     o_ref, _ = ref.cross_attention_fwd(f64(qb), f64(kb), f64(vb), [64])
     compare(dev_to_f64(o), o_ref, "xattn O after recovery")
+
+
+def test_timeout_in_backward():
+    grid, B, H = (2, 8, 16), 1, 1
+    shape = (B, 256, H, 128)
+    qb, kb, vb, dob = [bits(9, s, shape) for s in (synth.STREAM_Q, synth.STREAM_K, synth.STREAM_V,
+                                                     synth.STREAM_DO)]
+    q, k, v, do = (to_dev(x) for x in (qb, kb, vb, dob))
+    o, lse = wan.attention_forward(q, k, v, grid)
+    assert wan.wan_get_device_status() == wan.WAN_OK
+    wan.check(wan.wan_debug_inject_stall(1, 100))
+    try:
+        wan.attention_backward(q, k, v, o, lse, do, grid)
+    finally:
+        wan.wan_debug_inject_stall(0, 100)
+    assert wan.wan_get_device_status() == wan.WAN_ERR_TIMEOUT
+    dq, dk, dv = wan.attention_backward(q, k, v, o, lse, do, grid)
+    assert wan.wan_get_device_status() == wan.WAN_OK
+    dq_r, dk_r, dv_r = ref.self_attention_bwd(f64(qb), f64(kb), f64(vb), f64(dob), grid)
+    compare(dev_to_f64(dq), dq_r, "dQ after recovery")
+    compare(dev_to_f64(dv), dv_r, "dV after recovery")
