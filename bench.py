@@ -151,6 +151,20 @@ def aggregate(units_per_rank: float, world: int, max_seconds: float) -> float:
 # Our arm
 
 
+def timing_pairs(torch, stream, n):
+    """n (start, stop) CUDA event pairs for the library's profiling hook.
+
+    torch creates an event's handle lazily on its first record, so each pair
+    is recorded once here; the library then re-records both around its main
+    kernel, and elapsed_time reads those later records.
+    """
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in pairs:
+        a.record(stream)
+        b.record(stream)
+    return pairs
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -187,7 +201,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     wan.check(wan.wan_get_device_status())
 
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    kev = timing_pairs(torch, stream, args.steps)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     barrier(world)
@@ -300,7 +314,7 @@ def extras(wan, torch, dev, peaks):
         for _ in range(warm):
             fn(None)
         torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        ev = timing_pairs(torch, stream, iters)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for i in range(iters):

@@ -156,9 +156,12 @@ def wan_get_device_status(stream=None) -> int:
 
 
 def wan_profile_set_events(start, stop) -> int:
-    """start/stop: torch.cuda.Event (created with enable_timing) or None."""
-    return load_library().wan_profile_set_events(None if start is None else start.cuda_event,
-                                                 None if stop is None else stop.cuda_event)
+    """start/stop: torch.cuda.Event (created with enable_timing and recorded
+    at least once, so that its handle exists) or None."""
+    handles = [None if e is None else e.cuda_event for e in (start, stop)]
+    if any(h == 0 for h in handles):
+        raise ValueError("wan_profile_set_events: event has no CUDA handle yet (record it once first)")
+    return load_library().wan_profile_set_events(*handles)
 
 
 def wan_debug_inject_stall(count: int, timeout_ms: int) -> int:

@@ -185,11 +185,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(rows + kTile * 4, a.drow + bh * a.Lpad + q0, kTile * 4, bar);
         issued[s] = use + 1;
       }
-      if (*abort) {
-        mbar_wait(&bars[kBarKV], 0, nullptr, to);
-        for (int s = 0; s < 2; ++s)
-          if (issued[s] > 0) mbar_wait(&bars[kBarQFull0 + s], (issued[s] - 1) & 1, nullptr, to);
-      }
+      // Every copy this warp issued lands before the CTA may exit.
+      mbar_wait(&bars[kBarKV], 0, nullptr, to);
+      for (int s = 0; s < 2; ++s)
+        if (issued[s] > 0) mbar_wait(&bars[kBarQFull0 + s], (issued[s] - 1) & 1, nullptr, to);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {

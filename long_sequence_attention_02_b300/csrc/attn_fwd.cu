@@ -182,12 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(dst + kHalfBytes, m, &bar_kv_full[slot], 64, h, row, b);
         issued[slot] = use + 1;
       }
-      if (*abort) {
-        // Let every copy still in flight land before shared memory is released.
-        for (int s = 0; s < kStages; ++s)
-          if (issued[s] > 0) mbar_wait(&bar_kv_full[s], (issued[s] - 1) & 1, nullptr, to);
-        for (int t = 0; t < kQTiles; ++t) mbar_wait(&bar_q_full[t], 0, nullptr, to);
-      }
+      // Every copy this warp issued lands before the CTA may exit (on the
+      // normal path the consumers already waited for all of them).
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s] > 0) mbar_wait(&bar_kv_full[s], (issued[s] - 1) & 1, nullptr, to);
+      for (int t = 0; t < kQTiles; ++t) mbar_wait(&bar_q_full[t], 0, nullptr, to);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
