@@ -161,6 +161,38 @@ int wan_profile_set_events(void* start, void* stop);
  */
 int wan_debug_inject_stall(int count, int timeout_ms);
 
+/*
+ * Allocation-free variant of wan_attn_fwd. The Wan pages have no counterpart
+ * of this entry point; it exists for callers that cannot allocate device
+ * memory themselves: a host framework or plugin interface that hands the
+ * library only its input and output buffers and offers no workspace, a
+ * process whose device memory is entirely held by another allocator, or a
+ * latency-critical caller that must not pay cudaMalloc's implicit device
+ * synchronisation.
+ *
+ * Arguments, layout, results and errors are those of wan_attn_fwd, without
+ * the workspace. The rotated keys go to a fixed scratch array that the
+ * library keeps in device memory (a file-scope __device__ array of
+ * WAN_NOALLOC_SCRATCH_BYTES = 64 MiB, held on every GPU that loads the
+ * library until the process exits). So:
+ *   - B * L * H must not exceed WAN_NOALLOC_MAX_ROW_HEADS (262,144, e.g. one
+ *     32,760-token video with 8 heads); larger problems return
+ *     WAN_ERR_INVALID before anything is enqueued;
+ *   - the library itself allocates nothing here (no cudaMalloc, cudaFree or
+ *     allocating library call);
+ *   - every call on a device shares the same scratch, which keeps the last
+ *     call's contents (each call overwrites all of the part it reads); two
+ *     calls whose work overlaps on the GPU (e.g. on two streams without an
+ *     ordering between them) race on it and give undefined results;
+ *   - the first call on each device looks up the scratch array's device
+ *     address (cudaGetSymbolAddress, with that device current); make that
+ *     first call before any stream capture on the device.
+ */
+#define WAN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+#define WAN_NOALLOC_MAX_ROW_HEADS (WAN_NOALLOC_SCRATCH_BYTES / 256u)
+int wan_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g,
+                         int H, int head_dim, const float* tables, float scale, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

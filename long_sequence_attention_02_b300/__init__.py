@@ -32,8 +32,10 @@ DEFAULT_THETA = 10000.0
 EXPORTED = (
     "wan_status_str", "wan_version", "wan_rope3d_tables_size", "wan_rope3d_tables",
     "wan_attn_workspace_size", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
-    "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall",
+    "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall", "wan_attn_fwd_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+NOALLOC_MAX_ROW_HEADS = NOALLOC_SCRATCH_BYTES // 256
 
 
 class WanError(RuntimeError):
@@ -68,11 +70,13 @@ def load_library(path: str = LIB_PATH):
     lib.wan_xattn_fwd.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, wan_grid_t, i32, i32, f32, vp]
     lib.wan_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, wan_grid_t, i32, i32, vp, f32, vp, sz,
                                  vp]
+    lib.wan_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, wan_grid_t, i32, i32, vp, f32, vp]
     lib.wan_get_device_status.argtypes = [vp]
     lib.wan_debug_inject_stall.argtypes = [i32, i32]
     lib.wan_profile_set_events.argtypes = [vp, vp]
     for name in ("wan_rope3d_tables", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
-                 "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall"):
+                 "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall",
+                 "wan_attn_fwd_noalloc"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -149,6 +153,13 @@ def wan_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, grid, H, head_dim, tables
     return load_library().wan_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                                        _ptr(dk), _ptr(dv), B, _grid(grid), H, head_dim, _ptr(tables), float(scale),
                                        _ptr(workspace), int(ws_bytes), _stream(stream))
+
+
+def wan_attn_fwd_noalloc(q, k, v, o, lse, B, grid, H, head_dim, tables, scale, stream=None) -> int:
+    """wan_attn_fwd without a workspace: the library's fixed device scratch
+    holds the rotated keys (B * L * H <= NOALLOC_MAX_ROW_HEADS)."""
+    return load_library().wan_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, _grid(grid), H,
+                                                head_dim, _ptr(tables), float(scale), _stream(stream))
 
 
 def wan_get_device_status(stream=None) -> int:

@@ -102,6 +102,28 @@ wan::RopeTables split_tables(const float* tables, wan_grid_t g) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Scratch of wan_attn_fwd_noalloc: the rotated keys of one call. Held on
+// every device that loads the library; its device address is looked up once
+// per device (noalloc_scratch below), since in host code the name is only a
+// host-side stand-in.
+static __device__ __align__(256) uint8_t g_wan_noalloc_scratch[WAN_NOALLOC_SCRATCH_BYTES];
+
+void* g_noalloc_addr[kMaxDevices];  // device address of the scratch, per device (guarded by g_mu)
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return WAN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return WAN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_wan_noalloc_scratch) != cudaSuccess || p == nullptr) return WAN_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return WAN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -243,6 +265,24 @@ int wan_profile_set_events(void* start, void* stop) {
   g_prof_start = static_cast<cudaEvent_t>(start);
   g_prof_stop = static_cast<cudaEvent_t>(stop);
   return WAN_OK;
+}
+
+int wan_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g,
+                         int H, int head_dim, const float* tables, float scale, void* stream) {
+  long long L = 0;
+  int rc = grid_tokens(g, &L);
+  if (rc == WAN_OK) rc = check_shapes(B, L, H, head_dim);
+  if (rc != WAN_OK) return rc;
+  // The rotated keys (B * L * H rows of 256 bytes) must fit the fixed scratch.
+  if ((unsigned long long)B * (unsigned long long)L * (unsigned long long)H > WAN_NOALLOC_MAX_ROW_HEADS)
+    return WAN_ERR_INVALID;
+  if (B == 0) return WAN_OK;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != WAN_OK) return rc;
+  void* scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch)) != WAN_OK) return rc;
+  return wan_attn_fwd(q, k, v, o, lse, B, g, H, head_dim, tables, scale, scratch, WAN_NOALLOC_SCRATCH_BYTES,
+                      stream);
 }
 
 int wan_debug_inject_stall(int count, int timeout_ms) {
