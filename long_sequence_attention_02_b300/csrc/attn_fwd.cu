@@ -11,10 +11,12 @@
 // right after it lands; keys arrive already rotated.
 //
 // CTA = 2 query tiles of 128 rows of one (b, h); loop over 128-key tiles.
-//   warps 0-3  softmax of query tile 0 (one thread per row)
-//   warps 4-7  softmax of query tile 1
-//   warp  8    TMA producer (Q once, then K_j, V_j into a 4-slot ring)
-//   warp  9    MMA issuer (one thread) and TMEM owner
+// Three warpgroups (register budgets moved with setmaxnreg):
+//   warps 0-3   softmax of query tile 0 (one thread per row)      216 regs
+//   warps 4-7   softmax of query tile 1                           216 regs
+//   warp  8     TMA producer (Q once, then K_j, V_j into a 4-slot ring)
+//   warp  9     MMA issuer (one thread) and TMEM owner
+//   warps 10-11 idle                                               72 regs
 // TMEM (512 columns x 128 lanes, fp32): S0 [0,128) S1 [128,256) O0 [256,384)
 // O1 [384,512). P_t (bf16, two per column) overwrites the first 64 columns of
 // S_t and is the A operand of O_t += P_t V_j straight from TMEM.
@@ -39,7 +41,9 @@ constexpr int kBlockN = 128;
 constexpr int kStages = 4;
 constexpr int kTileBytes = 128 * 128 * 2;
 constexpr int kHalfBytes = kTileBytes / 2;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr uint32_t kSoftmaxRegs = 216;  // 2 x 128 x 216 + 128 x 72 = 384 x 168
+constexpr uint32_t kControlRegs = 72;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kSmemBytes = (kQTiles + kStages) * kTileBytes + 1024;
@@ -153,7 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp == kLoadWarp) {
+  if (warp >= 8) {
+   regs_shrink<kControlRegs>();
+   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -255,7 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&bar_drain, 0, nullptr, to);
     }
     __syncwarp();
+   }
   } else {
+    regs_grow<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;
     const int wq = warp & 3;
@@ -282,20 +290,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
       tmem_ld_wait();
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sr[c][i]);
+#define WAN_S(e) __uint_as_float(sr[(e) >> 5][(e) & 31])
       const int valid = n_valid - j * kBlockN;
       if (valid < kBlockN) {
 #pragma unroll
         for (int i = 0; i < 128; ++i)
-          if (i >= valid) s[i] = -INFINITY;
+          if (i >= valid) sr[i >> 5][i & 31] = __float_as_uint(-INFINITY);
       }
-      float mx = s[0];
+      // Row max: four independent chains of three-input maxima.
+      float mc[4];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+      for (int q = 0; q < 4; ++q) mc[q] = WAN_S(q);
+#pragma unroll
+      for (int i = 4; i < 128; i += 8) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          mc[q] = max3f(mc[q], WAN_S(i + 2 * q), WAN_S(i + 2 * q + 1));
+      }
+      const float mx = max3f(mc[0], mc[1], fmaxf(mc[2], mc[3]));
       const float m_new = fmaxf(m_ref, mx);
       if (j == 0) {
         m_ref = m_new;
@@ -318,20 +330,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // p = 2^(s * scale * log2(e) - m * scale * log2(e)), two lanes per f32x2 op.
       const float neg = -m_ref * sl2;
-      float lsum = 0.f;
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      const uint64_t negx2 = f2_pack(neg, neg);
+      uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, neg));
-          const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, neg));
-          lsum += p0 + p1;
+          const int e = c * 32 + 2 * i;
+          const uint64_t x = f2_fma(f2_pack(WAN_S(e), WAN_S(e + 1)), sl2x2, negx2);
+          float x0, x1;
+          f2_unpack(x, x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          const uint64_t pp = f2_pack(p0, p1);
+          acc[i & 1] = f2_add(acc[i & 1], pp);
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + c * 16, pk);
       }
+      float a0, a1, a2, a3;
+      f2_unpack(acc[0], a0, a1);
+      f2_unpack(acc[1], a2, a3);
+      const float lsum = (a0 + a1) + (a2 + a3);
+#undef WAN_S
       l += lsum;
       tmem_st_wait();
       tc_fence_before();
