@@ -12,11 +12,11 @@
 //
 // CTA = 2 query tiles of 128 rows of one (b, h); loop over 128-key tiles.
 // Three warpgroups (register budgets moved with setmaxnreg):
-//   warps 0-3   softmax of query tile 0 (one thread per row)      216 regs
-//   warps 4-7   softmax of query tile 1                           216 regs
+//   warps 0-3   softmax of query tile 0 (one thread per row)      208 regs
+//   warps 4-7   softmax of query tile 1                           208 regs
 //   warp  8     TMA producer (Q once, then K_j, V_j into a 4-slot ring)
 //   warp  9     MMA issuer (one thread) and TMEM owner
-//   warps 10-11 idle                                               72 regs
+//   warps 10-11 idle                                               88 regs
 // TMEM (512 columns x 128 lanes, fp32): S0 [0,128) S1 [128,256) O0 [256,384)
 // O1 [384,512). P_t (bf16, two per column) overwrites the first 64 columns of
 // S_t and is the A operand of O_t += P_t V_j straight from TMEM.
@@ -42,8 +42,8 @@ constexpr int kStages = 4;
 constexpr int kTileBytes = 128 * 128 * 2;
 constexpr int kHalfBytes = kTileBytes / 2;
 constexpr int kThreads = 384;
-constexpr uint32_t kSoftmaxRegs = 216;  // 2 x 128 x 216 + 128 x 72 = 384 x 168
-constexpr uint32_t kControlRegs = 72;
+constexpr uint32_t kSoftmaxRegs = 208;  // 2 x 128 x 208 + 128 x 88 = 384 x 168
+constexpr uint32_t kControlRegs = 88;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kSmemBytes = (kQTiles + kStages) * kTileBytes + 1024;
@@ -197,67 +197,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop (waits and descriptor arithmetic are
+    // warp-uniform); one elected lane issues each MMA and commit.
+    {
       const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // Q (K-major) x K (K-major)
       const uint32_t idesc_o = idesc_bf16_f32(128, 128, 0, 1);  // P (TMEM) x V (MN-major)
-      const uint32_t sq = smem_u32(sQ);
-      const uint32_t skv = smem_u32(sKV);
+      // Descriptors of the tiles' first K=16 slices; the others add a
+      // constant to the start-address field (16-byte units).
+      const uint64_t dq0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dkv_k = sdesc_sw128(smem_u32(sKV), 16, 1024);
+      const uint64_t dkv_v = sdesc_sw128(smem_u32(sKV), kHalfBytes, 1024);
       auto issue_qk = [&](int t, int slot) {
-        const uint32_t qa = sq + t * kTileBytes;
-        const uint32_t ka = skv + slot * kTileBytes;
+        const uint64_t qd = dq0 + static_cast<uint64_t>(t * (kTileBytes >> 4));
+        const uint64_t kd = dkv_k + static_cast<uint64_t>(slot * (kTileBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          umma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_s,
-                  kk > 0);
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+          umma_ss_elect(tmem + t * 128, qd + off, kd + off, idesc_s, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint32_t va = skv + slot * kTileBytes;
+        const uint64_t vd = dkv_v + static_cast<uint64_t>(slot * (kTileBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, sdesc_sw128(va + kk * 2048, kHalfBytes, 1024),
-                  idesc_o, (acc || kk > 0) ? 1u : 0u);
+          umma_ts_elect(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, vd + static_cast<uint64_t>(kk * (2048 >> 4)),
+                        idesc_o, (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = true;
-      for (int t = 0; t < kQTiles && ok; ++t) ok = mbar_wait(&bar_q_ready[t], 0, abort, to);
+      for (int t = 0; t < kQTiles && ok; ++t) ok = warp_wait(&bar_q_ready[t], 0, abort, a.lc.err, to);
       if (ok && n_tiles > 0) {
-        ok = mbar_wait(&bar_kv_full[0], 0, abort, to);
+        ok = warp_wait(&bar_kv_full[0], 0, abort, a.lc.err, to);
         if (ok) {
           tc_fence_after();
           issue_qk(0, 0);
-          umma_commit(&bar_s_full[0]);
+          umma_commit_elect(&bar_s_full[0]);
           issue_qk(1, 0);
-          umma_commit(&bar_s_full[1]);
-          umma_commit(&bar_kv_empty[0]);
+          umma_commit_elect(&bar_s_full[1]);
+          umma_commit_elect(&bar_kv_empty[0]);
         }
         for (int j = 0; j < n_tiles && ok; ++j) {
           const int iv = 2 * j + 1;
           const int vslot = iv % kStages;
-          ok = mbar_wait(&bar_kv_full[vslot], (iv / kStages) & 1, abort, to);
+          ok = warp_wait(&bar_kv_full[vslot], (iv / kStages) & 1, abort, a.lc.err, to);
           const bool has_next = j + 1 < n_tiles;
           const int ik = 2 * j + 2;
           const int kslot = ik % kStages;
-          if (ok && has_next) ok = mbar_wait(&bar_kv_full[kslot], (ik / kStages) & 1, abort, to);
+          if (ok && has_next) ok = warp_wait(&bar_kv_full[kslot], (ik / kStages) & 1, abort, a.lc.err, to);
           for (int t = 0; t < kQTiles && ok; ++t) {
-            ok = mbar_wait(&bar_p_full[t], j & 1, abort, to);
+            ok = warp_wait(&bar_p_full[t], j & 1, abort, a.lc.err, to);
             if (!ok) break;
             tc_fence_after();
             issue_pv(t, vslot, j > 0);
-            if (t == kQTiles - 1) umma_commit(&bar_kv_empty[vslot]);
+            if (t == kQTiles - 1) umma_commit_elect(&bar_kv_empty[vslot]);
             if (!has_next) {
-              umma_commit(&bar_o_full[t]);
+              umma_commit_elect(&bar_o_full[t]);
             } else {
               issue_qk(t, kslot);
-              umma_commit(&bar_s_full[t]);
-              if (t == kQTiles - 1) umma_commit(&bar_kv_empty[kslot]);
+              umma_commit_elect(&bar_s_full[t]);
+              if (t == kQTiles - 1) umma_commit_elect(&bar_kv_empty[kslot]);
             }
           }
         }
       }
-      if (!ok) raise_abort(abort, a.lc.err);
       // Every MMA of this CTA must be done before TMEM is released.
-      umma_commit(&bar_drain);
+      umma_commit_elect(&bar_drain);
       mbar_wait(&bar_drain, 0, nullptr, to);
     }
     __syncwarp();
