@@ -25,8 +25,14 @@
 //      them are ordered before (tcgen05 MMAs of one thread run in order).
 //      Epilogue: dV -> bf16; dK -> R^T -> bf16.
 //   3. post: dQ = R^T dQ_acc -> bf16.
-// Warps: 0-7 compute (warp w: TMEM lanes 32*(w%4).., column half w/4),
-// 8 TMA producer, 9 MMA issuer and TMEM owner.
+//      The fp32 reduction of dQ into global memory is the costly part of the
+//      backward (one 64 KB tile per query tile per CTA); it is done by a
+//      warpgroup of its own so that it overlaps the next tile's softmax.
+// Warps (register budgets moved with setmaxnreg):
+//   0-7    compute (warp w: TMEM lanes 32*(w%4).., column half w/4)   160 regs
+//   8      TMA producer; 9 MMA issuer (warp-converged, one elected lane
+//          issues) and TMEM owner; 10-11 idle                           112 regs
+//   12-15  dQ writers (warp w: TMEM lanes 32*(w%4)..)                    80 regs
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -34,7 +40,11 @@ namespace wan {
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 512;
+constexpr uint32_t kComputeRegs = 160;  // 2 x 128 x 160 + 128 x 112 + 128 x 80 = 512 x 128
+constexpr uint32_t kControlRegs = 112;
+constexpr uint32_t kDqRegs = 80;
+constexpr int kDqWarp0 = 12;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTile = 128;
@@ -49,7 +59,7 @@ constexpr int kOffDS = kOffStage + 2 * kStageBytes;
 constexpr int kOffRows = kOffDS + kTileBytes;  // 2 stages of {LSE*log2e[128], D[128]}
 constexpr int kRowsBytes = 2 * kTile * 4;
 constexpr int kOffBar = kOffRows + 2 * kRowsBytes;
-constexpr int kSmemBytes = kOffBar + 256;
+constexpr int kSmemBytes = kOffBar + 256;  // barriers [0,112), TMEM base, abort word, dQ stop flags at 128
 
 enum Bar {
   kBarKV = 0,
@@ -63,8 +73,10 @@ enum Bar {
   kBarDQFree = 10,
   kBarAcc = 11,
   kBarDrain = 12,
-  kNumBars = 13
+  kBarDSFree = 13,  // the dS buffer, used as dQ staging after the dQ MMA, is free again
+  kNumBars = 14
 };
+static_assert(kNumBars * 8 + 8 <= 128, "barrier area overlaps the dQ stop flags");
 
 struct BwdArgs {
   const float* lse2;  // [B*H][Lpad] LSE * log2(e), pad +inf
@@ -102,7 +114,7 @@ __device__ __forceinline__ void load32(uint32_t taddr, float (&v)[32]) {
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const BwdArgs a) {
+                    const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(smem + kOffBar + kNumBars * 8);
@@ -115,6 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = blockIdx.z;
   const int kv0 = blockIdx.x * kTile;
   const int nq = (a.L + kTile - 1) / kTile;
+  // Query tiles are visited from a per-CTA starting tile, so that the CTAs of
+  // one head in flight add their dQ contributions into different rows
+  // instead of all contending for the same L2 lines.
+  const int q_start = static_cast<int>((static_cast<long long>(blockIdx.x) * nq) / gridDim.x);
   const uint64_t to = a.lc.timeout_ns;
 
   // The tile math below needs a 1024-byte aligned base (128B swizzle atoms).
@@ -134,9 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kBarP], 8);
     mbar_init(&bars[kBarDS], 8);
     mbar_init(&bars[kBarDQ], 1);
-    mbar_init(&bars[kBarDQFree], 8);
+    mbar_init(&bars[kBarDQFree], 4);
     mbar_init(&bars[kBarAcc], 1);
     mbar_init(&bars[kBarDrain], 1);
+    mbar_init(&bars[kBarDSFree], 1);
     *abort_sh = 0;
     fence_mbar_init();
   }
@@ -152,7 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const size_t bh = static_cast<size_t>(b) * a.H + h;
 
-  if (warp == kLoadWarp) {
+  if (warp >= 8 && warp < kDqWarp0) {
+   regs_shrink<kControlRegs>();
+   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -176,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* rows = smem + kOffRows + s * kRowsBytes;
         uint64_t* bar = &bars[kBarQFull0 + s];
         mbar_arrive_expect_tx(bar, 2 * kTileBytes + kRowsBytes);
-        const int q0 = i * kTile;
+        const int q0 = (i + q_start < nq ? i + q_start : i + q_start - nq) * kTile;
         tma_load_4d(st, &tm_q, bar, 0, h, q0, b);
         tma_load_4d(st + kHalfBytes, &tm_q, bar, 64, h, q0, b);
         tma_load_4d(st + kTileBytes, &tm_do, bar, 0, h, q0, b);
@@ -191,65 +210,121 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (issued[s] > 0) mbar_wait(&bars[kBarQFull0 + s], (issued[s] - 1) & 1, nullptr, to);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {
       const uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
       const uint32_t id_tm = idesc_bf16_f32(128, 128, 0, 1);  // A from TMEM, B MN-major
       const uint32_t id_dq = idesc_bf16_f32(128, 64, 1, 1);   // A and B MN-major, N = 64
-      const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
-      const uint32_t sDS = smem_u32(smem + kOffDS);
-      bool ok = mbar_wait(&bars[kBarKV], 0, abort, to);
+      const uint64_t dK = sdesc_sw128(smem_u32(smem + kOffK), 16, 1024);
+      const uint64_t dV = sdesc_sw128(smem_u32(smem + kOffV), 16, 1024);
+      const uint64_t dKmn = sdesc_sw128(smem_u32(smem + kOffK), kHalfBytes, 1024);
+      const uint64_t dDS = sdesc_sw128(smem_u32(smem + kOffDS), kHalfBytes, 1024);
+      const uint64_t dStage_k = sdesc_sw128(smem_u32(smem + kOffStage), 16, 1024);
+      const uint64_t dStage_mn = sdesc_sw128(smem_u32(smem + kOffStage), kHalfBytes, 1024);
+      bool ok = warp_wait(&bars[kBarKV], 0, abort, a.lc.err, to);
       for (int i = 0; i < nq && ok; ++i) {
         const int s = i & 1, use = i >> 1;
-        const uint32_t sQ = smem_u32(smem + kOffStage + s * kStageBytes);
-        const uint32_t sDO = sQ + kTileBytes;
-        ok = mbar_wait(&bars[kBarQFull0 + s], use & 1, abort, to);
-        if (ok && i > 0) ok = mbar_wait(&bars[kBarDQFree], (i - 1) & 1, abort, to);
+        const uint64_t so = static_cast<uint64_t>((s * kStageBytes) >> 4);   // Q tile of stage s
+        const uint64_t sdo = so + static_cast<uint64_t>(kTileBytes >> 4);      // dO tile of stage s
+        ok = warp_wait(&bars[kBarQFull0 + s], use & 1, abort, a.lc.err, to);
+        if (ok && i > 0) ok = warp_wait(&bars[kBarDQFree], (i - 1) & 1, abort, a.lc.err, to);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          umma_ss(tS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), id_kk, kk > 0);
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+          umma_ss_elect(tS, dK + off, dStage_k + so + off, id_kk, kk > 0);
         }
-        umma_commit(&bars[kBarS]);
+        umma_commit_elect(&bars[kBarS]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          umma_ss(tDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), id_kk, kk > 0);
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+          umma_ss_elect(tDP, dV + off, dStage_k + sdo + off, id_kk, kk > 0);
         }
-        umma_commit(&bars[kBarDP]);
-        if (!(ok = mbar_wait(&bars[kBarP], i & 1, abort, to))) break;
+        umma_commit_elect(&bars[kBarDP]);
+        if (!(ok = warp_wait(&bars[kBarP], i & 1, abort, a.lc.err, to))) break;
         tc_fence_after();
         // P^T sits in S columns [0,32) (queries 0..63) and [64,96) (queries 64..127).
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tDV, tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(sDO + kk * 2048, kHalfBytes, 1024), id_tm,
-                  (i > 0 || kk > 0) ? 1u : 0u);
-        if (!(ok = mbar_wait(&bars[kBarDS], i & 1, abort, to))) break;
+          umma_ts_elect(tDV, tS + (kk >> 2) * 64 + (kk & 3) * 8, dStage_mn + sdo + static_cast<uint64_t>(kk * 128),
+                        id_tm, (i > 0 || kk > 0) ? 1u : 0u);
+        if (!(ok = warp_wait(&bars[kBarDS], i & 1, abort, a.lc.err, to))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tDK, tDP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(sQ + kk * 2048, kHalfBytes, 1024), id_tm,
-                  (i > 0 || kk > 0) ? 1u : 0u);
+          umma_ts_elect(tDK, tDP + (kk >> 2) * 64 + (kk & 3) * 8, dStage_mn + so + static_cast<uint64_t>(kk * 128),
+                        id_tm, (i > 0 || kk > 0) ? 1u : 0u);
         // dQ_i = dS K_rot, d-halves into S[64,128) and dP[64,128).
 #pragma unroll
         for (int half = 0; half < 2; ++half)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_ss((half ? tDP : tS) + 64, sdesc_sw128(sDS + kk * 2048, kHalfBytes, 1024),
-                    sdesc_sw128(sK + half * kHalfBytes + kk * 2048, kHalfBytes, 1024), id_dq, kk > 0);
-        umma_commit(&bars[kBarDQ]);
-        umma_commit(&bars[kBarQEmpty0 + s]);
+            umma_ss_elect((half ? tDP : tS) + 64, dDS + static_cast<uint64_t>(kk * 128),
+                          dKmn + static_cast<uint64_t>((half * kHalfBytes + kk * 2048) >> 4), id_dq, kk > 0);
+        umma_commit_elect(&bars[kBarDQ]);
+        umma_commit_elect(&bars[kBarQEmpty0 + s]);
       }
-      if (ok) umma_commit(&bars[kBarAcc]);
-      if (!ok) raise_abort(abort, a.lc.err);
-      umma_commit(&bars[kBarDrain]);
+      if (ok) umma_commit_elect(&bars[kBarAcc]);
+      umma_commit_elect(&bars[kBarDrain]);
       mbar_wait(&bars[kBarDrain], 0, nullptr, to);
     }
-    __syncwarp();
+   }
+  } else if (warp >= kDqWarp0) {
+    regs_shrink<kDqRegs>();
+    // ------------------------------------------------------------ dQ writers
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
+    // Per-warp stop flags (in the dynamic barrier area: a static __shared__
+    // array would move the 1024-byte aligned dynamic base).
+    volatile int* dq_fail = reinterpret_cast<volatile int*>(smem + kOffBar + 128);
+    for (int i = 0; i < nq; ++i) {
+      const bool ok = warp_wait(&bars[kBarDQ], i & 1, abort, a.lc.err, to);
+      // The four warps decide together whether to stop, so that none of
+      // them is left waiting at the named barriers below.
+      if (lane == 0) dq_fail[wq] = ok ? 0 : 1;
+      named_bar_sync(1, 128);
+      if (dq_fail[0] | dq_fail[1] | dq_fail[2] | dq_fail[3]) break;
+      tc_fence_after();
+      // dQ leaves TMEM in two halves of 64 columns. Each half is staged in the
+      // dS buffer (free once the dQ MMAs have completed) as two 128-row x
+      // 32-float boxes in the 128-byte swizzled layout, then one elected
+      // thread adds the boxes to the fp32 accumulator with bulk tensor
+      // reductions and waits until they have read the staging buffer.
+      const int qt = i + q_start < nq ? i + q_start : i + q_start - nq;
+      uint8_t* stage = smem + kOffDS;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[64];
+        tmem_ld32((half ? tDP : tS) + lane_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32((half ? tDP : tS) + lane_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_ld_wait();
+        if (half == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kBarDQFree]);
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c)  // box c/8, 16-byte chunk c%8 of row r
+          *reinterpret_cast<uint4*>(stage + (c >> 3) * (kTile * 128) + sw128_offset(r, c & 7)) =
+              make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (warp == kDqWarp0 && lane == 0) {
+          tma_reduce_add_4d(&tm_dq, stage, half * 64, h, qt * kTile, b);
+          tma_reduce_add_4d(&tm_dq, stage + kTile * 128, half * 64 + 32, h, qt * kTile, b);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          if (half == 1) mbar_arrive(&bars[kBarDSFree]);
+        }
+        named_bar_sync(1, 128);
+      }
+    }
+    if (warp == kDqWarp0 && lane == 0) bulk_wait_group0();
   } else {
+    regs_grow<kComputeRegs>();
     // ------------------------------------------------------------ compute
     const int wq = warp & 3;
     const int ch = warp >> 2;  // column half
@@ -306,6 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st32(tDP + lane_addr + ch * 64, pk);
         // dS^T row r, queries ch*64 .. ch*64+63 -> half tile ch of the MN-major A operand.
+        // The dS buffer doubles as the dQ staging area of the previous tile.
+        if (i > 0 && !(ok = warp_wait(&bars[kBarDSFree], (i - 1) & 1, abort, a.lc.err, to))) {
+          tmem_st_wait();
+          break;
+        }
         uint8_t* ds_row = smem + kOffDS + ch * kHalfBytes;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc)
@@ -318,29 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarDS]);
 
-      if (!(ok = warp_wait(&bars[kBarDQ], i & 1, abort, a.lc.err, to))) break;
-      tc_fence_after();
-      float dq[64];
-      {
-        float t32[32];
-        load32((ch ? tDP : tS) + lane_addr + 64, t32);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) dq[k] = t32[k];
-        load32((ch ? tDP : tS) + lane_addr + 96, t32);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) dq[32 + k] = t32[k];
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarDQFree]);
-      const int qrow = i * kTile + r;  // TMEM lane = query row of this tile
-      if (qrow < a.L) {
-        float4* dst = reinterpret_cast<float4*>(a.dq_acc + ((static_cast<size_t>(b) * a.L + qrow) * a.H + h) * 128 +
-                                                ch * 64);
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-          atomicAdd(dst + k, make_float4(dq[4 * k], dq[4 * k + 1], dq[4 * k + 2], dq[4 * k + 3]));
-      }
     }
     // ------------------------------------------------------------ epilogue
     if (ok) ok = warp_wait(&bars[kBarAcc], 0, abort, a.lc.err, to);
@@ -500,9 +557,10 @@ int launch_attn_bwd(const void* q, const void* k, const void* v, const void* o, 
   }
   if (cudaMemsetAsync(w.dq_acc, 0, (size_t)n_rows * 512, s) != cudaSuccess) return WAN_ERR_CUDA;
 
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_tmap_bld(&tq, w.q_rot, B, L, H, kHeadDim, 128) || !make_tmap_bld(&tk, w.k_rot, B, L, H, kHeadDim, 128) ||
-      !make_tmap_bld(&tv, v, B, L, H, kHeadDim, 128) || !make_tmap_bld(&tdo, dout, B, L, H, kHeadDim, 128))
+      !make_tmap_bld(&tv, v, B, L, H, kHeadDim, 128) || !make_tmap_bld(&tdo, dout, B, L, H, kHeadDim, 128) ||
+      !make_tmap_f32_bld(&tdq, w.dq_acc, B, L, H, kHeadDim, 128))
     return WAN_ERR_CUDA;
   BwdArgs a;
   a.lse2 = w.lse2;
@@ -523,7 +581,7 @@ int launch_attn_bwd(const void* q, const void* k, const void* v, const void* o, 
     return WAN_ERR_CUDA;
   dim3 grid((L + kTile - 1) / kTile, H, B);
   record_start(lc, s);
-  attn_bwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, a);
+  attn_bwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, tdo, tdq, a);
   record_stop(lc, s);
   if (cudaGetLastError() != cudaSuccess) return WAN_ERR_CUDA;
   if (launch_rope_unrotate_f32(w.dq_acc, dq, B, g, H, tab, s) != cudaSuccess) return WAN_ERR_CUDA;
