@@ -10,24 +10,33 @@
 // With 3D RoPE (same page, DiT 块) the query tile is rotated in shared memory
 // right after it lands; keys arrive already rotated.
 //
-// CTA = 2 query tiles of 128 rows of one (b, h); loop over 128-key tiles.
+// Persistent CTAs (one per SM) walk a static list of work items; an item is
+// 2 query tiles of 128 rows of one (b, h), processed against all key tiles.
 // Three warpgroups (register budgets moved with setmaxnreg):
 //   warps 0-3   softmax of query tile 0 (one thread per row)      208 regs
 //   warps 4-7   softmax of query tile 1                           208 regs
-//   warp  8     TMA producer (Q once, then K_j, V_j into a 4-slot ring)
-//   warp  9     MMA issuer (one thread) and TMEM owner
+//   warp  8     TMA producer (Q per item, then K_j, V_j into a ring)
+//   warp  9     MMA issuer (warp-converged, one elected lane) and TMEM owner
 //   warps 10-11 idle                                               88 regs
+// Cross-attention items are short (at most 4 key tiles), so there Q is
+// double-buffered: the next item's Q load and first QK overlap the current
+// item's output epilogue. Self-attention uses one Q buffer and a 4-slot ring.
 // TMEM (512 columns x 128 lanes, fp32): S0 [0,128) S1 [128,256) O0 [256,384)
 // O1 [384,512). P_t (bf16, two per column) overwrites the first 64 columns of
 // S_t and is the A operand of O_t += P_t V_j straight from TMEM.
+// Each item visits its key tiles cyclically from an item-dependent start.
 // Per key tile the MMA order is PV0(j), QK0(j+1), PV1(j), QK1(j+1): softmax of
 // tile 0 for j+1 overlaps the tensor work of tile 1 and vice versa. Because
 // tcgen05 MMAs from one thread run in issue order, QK_t(j+1) never overwrites
 // P_t(j) before PV_t(j) has read it, and O_t is final for iteration j once
-// S_t(j+1) is signalled.
+// S_t(j+1) is signalled. The same ordering lets an item's first PV, which
+// overwrites O_t, follow the previous item's epilogue: the softmax warps read
+// O_t out of TMEM before they signal the new item's first P.
 // Softmax keeps a per-row reference max m and rescales O (in TMEM) and l only
 // when the tile max exceeds m by more than 2^8 in the exp2 domain; the final
 // O / l is exact for any reference, and p <= 256 stays well inside bf16.
+#include <climits>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -38,7 +47,6 @@ namespace {
 constexpr int kBlockM = 128;
 constexpr int kQTiles = 2;
 constexpr int kBlockN = 128;
-constexpr int kStages = 4;
 constexpr int kTileBytes = 128 * 128 * 2;
 constexpr int kHalfBytes = kTileBytes / 2;
 constexpr int kThreads = 384;
@@ -46,7 +54,13 @@ constexpr uint32_t kSoftmaxRegs = 208;  // 2 x 128 x 208 + 128 x 88 = 384 x 168
 constexpr uint32_t kControlRegs = 88;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kSmemBytes = (kQTiles + kStages) * kTileBytes + 1024;
+// Q buffers and K/V ring slots (self-attention: 1 + 4, cross-attention: 2 + 3).
+template <bool kRope>
+struct FwdCfg {
+  static constexpr int kQBuf = kRope ? 1 : 2;
+  static constexpr int kStages = kRope ? 4 : 3;
+  static constexpr int kSmemBytes = (kQBuf * kQTiles + kStages) * kTileBytes + 1024;
+};
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct FwdArgs {
@@ -54,7 +68,8 @@ struct FwdArgs {
   float* lse;
   const int32_t* kv_lens;
   RopeTables tab;
-  int Lq, Lk, H, Hp, Wp;
+  int Lq, Lk, H, Hp, Wp, B;
+  int n_qpairs;  // 256-row query blocks per (b, h)
   float scale_log2;
   LaunchCommon lc;
 };
@@ -105,12 +120,14 @@ template <bool kRope>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+  constexpr int kQBuf = FwdCfg<kRope>::kQBuf;
+  constexpr int kStages = FwdCfg<kRope>::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sKV = smem + kQTiles * kTileBytes;
+  uint8_t* sQ = smem;                                    // [kQBuf][2 tiles]
+  uint8_t* sKV = smem + kQBuf * kQTiles * kTileBytes;    // [kStages] tiles
 
-  __shared__ __align__(8) uint64_t bar_q_full[kQTiles], bar_q_ready[kQTiles];
+  __shared__ __align__(8) uint64_t bar_q_full[kQBuf], bar_q_ready[kQBuf], bar_q_empty[kQBuf];
   __shared__ __align__(8) uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
   __shared__ __align__(8) uint64_t bar_s_full[kQTiles], bar_p_full[kQTiles], bar_o_full[kQTiles];
   __shared__ __align__(8) uint64_t bar_drain;
@@ -119,23 +136,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
-  const int q0 = blockIdx.x * (kBlockM * kQTiles);
   const uint64_t to = a.lc.timeout_ns;
   volatile int* abort = &abort_sh;
+  const int n_items = a.n_qpairs * a.H * a.B;
 
-  int n_valid = a.Lk;
-  if (a.kv_lens != nullptr) {
-    const int v = a.kv_lens[b];
-    n_valid = v < 0 ? 0 : (v > a.Lk ? a.Lk : v);
-  }
-  const int n_tiles = (n_valid + kBlockN - 1) / kBlockN;
+  // Work item -> (b, h, first query row, key tiles, first key tile). Every
+  // role walks the same items, so all derive the same counters from them.
+  struct Item {
+    int b, h, q0, n_valid, n_tiles, kv_start;
+  };
+  auto item_of = [&](int it) {
+    Item x;
+    const int qp = it % a.n_qpairs;
+    const int bh = it / a.n_qpairs;
+    x.h = bh % a.H;
+    x.b = bh / a.H;
+    x.q0 = qp * (kBlockM * kQTiles);
+    x.n_valid = a.Lk;
+    if (a.kv_lens != nullptr) {
+      const int v = a.kv_lens[x.b];
+      x.n_valid = v < 0 ? 0 : (v > a.Lk ? a.Lk : v);
+    }
+    x.n_tiles = (x.n_valid + kBlockN - 1) / kBlockN;
+    // Key tiles are visited from a per-item offset (online softmax does not
+    // depend on the order), so that the CTAs of one head in flight read
+    // different K/V tiles.
+    x.kv_start = x.n_tiles > 0 ? static_cast<int>((static_cast<long long>(qp) * x.n_tiles) / a.n_qpairs) : 0;
+    return x;
+  };
 
   if (threadIdx.x == 0) {
+    for (int q = 0; q < kQBuf; ++q) {
+      mbar_init(&bar_q_full[q], 1);
+      mbar_init(&bar_q_ready[q], kRope ? 8 : 1);
+      mbar_init(&bar_q_empty[q], 1);
+    }
     for (int t = 0; t < kQTiles; ++t) {
-      mbar_init(&bar_q_full[t], 1);
-      mbar_init(&bar_q_ready[t], 4);
       mbar_init(&bar_s_full[t], 1);
       mbar_init(&bar_p_full[t], 4);
       mbar_init(&bar_o_full[t], 1);
@@ -165,37 +201,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      for (int t = 0; t < kQTiles; ++t) {
-        mbar_arrive_expect_tx(&bar_q_full[t], kTileBytes);
-        tma_load_4d(sQ + t * kTileBytes, &tm_q, &bar_q_full[t], 0, h, q0 + t * kBlockM, b);
-        tma_load_4d(sQ + t * kTileBytes + kHalfBytes, &tm_q, &bar_q_full[t], 64, h, q0 + t * kBlockM, b);
-      }
-      int issued[kStages];
-      for (int s = 0; s < kStages; ++s) issued[s] = 0;
-      for (int i = 0; i < 2 * n_tiles; ++i) {
-        const int slot = i % kStages;
-        const int use = i / kStages;
-        if (use > 0 && !mbar_wait(&bar_kv_empty[slot], (use - 1) & 1, abort, to)) {
+      int nq = 0;  // items whose Q was loaded
+      int ig = 0;  // K/V tiles issued (ring position)
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const Item x = item_of(it);
+        if (x.n_tiles == 0) continue;
+        const int qb = nq % kQBuf;
+        if (nq >= kQBuf && !mbar_wait(&bar_q_empty[qb], ((nq / kQBuf) - 1) & 1, abort, to)) {
           raise_abort(abort, a.lc.err);
           break;
         }
-        if (a.lc.stall && i == 1) continue;  // test hook: V_0 never arrives
-        const CUtensorMap* m = (i & 1) ? &tm_v : &tm_k;
-        const int row = (i >> 1) * kBlockN;
-        uint8_t* dst = sKV + slot * kTileBytes;
-        mbar_arrive_expect_tx(&bar_kv_full[slot], kTileBytes);
-        tma_load_4d(dst, m, &bar_kv_full[slot], 0, h, row, b);
-        tma_load_4d(dst + kHalfBytes, m, &bar_kv_full[slot], 64, h, row, b);
-        issued[slot] = use + 1;
+        uint8_t* qdst = sQ + qb * (kQTiles * kTileBytes);
+        mbar_arrive_expect_tx(&bar_q_full[qb], kQTiles * kTileBytes);
+        for (int t = 0; t < kQTiles; ++t) {
+          tma_load_4d(qdst + t * kTileBytes, &tm_q, &bar_q_full[qb], 0, x.h, x.q0 + t * kBlockM, x.b);
+          tma_load_4d(qdst + t * kTileBytes + kHalfBytes, &tm_q, &bar_q_full[qb], 64, x.h, x.q0 + t * kBlockM, x.b);
+        }
+        ++nq;
+        for (int i = 0; i < 2 * x.n_tiles; ++i, ++ig) {
+          const int slot = ig % kStages;
+          const int use = ig / kStages;
+          if (use > 0 && !mbar_wait(&bar_kv_empty[slot], (use - 1) & 1, abort, to)) {
+            raise_abort(abort, a.lc.err);
+            ok = false;
+            break;
+          }
+          if (a.lc.stall && ig == 1) continue;  // test hook: V_0 never arrives
+          const CUtensorMap* m = (i & 1) ? &tm_v : &tm_k;
+          const int jt = (i >> 1) + x.kv_start;
+          const int row = (jt < x.n_tiles ? jt : jt - x.n_tiles) * kBlockN;
+          uint8_t* dst = sKV + slot * kTileBytes;
+          mbar_arrive_expect_tx(&bar_kv_full[slot], kTileBytes);
+          tma_load_4d(dst, m, &bar_kv_full[slot], 0, x.h, row, x.b);
+          tma_load_4d(dst + kHalfBytes, m, &bar_kv_full[slot], 64, x.h, row, x.b);
+        }
       }
       // Every copy this warp issued lands before the CTA may exit (on the
-      // normal path the consumers already waited for all of them).
-      for (int s = 0; s < kStages; ++s)
-        if (issued[s] > 0) mbar_wait(&bar_kv_full[s], (issued[s] - 1) & 1, nullptr, to);
-      for (int t = 0; t < kQTiles; ++t) mbar_wait(&bar_q_full[t], 0, nullptr, to);
+      // normal path the consumers already waited for all of them). The last
+      // fill of each slot / buffer is that barrier's latest phase.
+      for (int k = ig - kStages < 0 ? 0 : ig - kStages; k < ig; ++k)
+        mbar_wait(&bar_kv_full[k % kStages], (k / kStages) & 1, nullptr, to);
+      for (int k = nq - kQBuf < 0 ? 0 : nq - kQBuf; k < nq; ++k)
+        mbar_wait(&bar_q_full[k % kQBuf], (k / kQBuf) & 1, nullptr, to);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop (waits and descriptor arithmetic are
     // warp-uniform); one elected lane issues each MMA and commit.
@@ -203,48 +254,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // Q (K-major) x K (K-major)
       const uint32_t idesc_o = idesc_bf16_f32(128, 128, 0, 1);  // P (TMEM) x V (MN-major)
       // Descriptors of the tiles' first K=16 slices; the others add a
-      // constant to the start-address field (16-byte units).
+      // constant to the start-address field (16-byte units, low word). All
+      // of them share the high word.
       const uint64_t dq0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dkv_k = sdesc_sw128(smem_u32(sKV), 16, 1024);
       const uint64_t dkv_v = sdesc_sw128(smem_u32(sKV), kHalfBytes, 1024);
-      auto issue_qk = [&](int t, int slot) {
-        const uint64_t qd = dq0 + static_cast<uint64_t>(t * (kTileBytes >> 4));
-        const uint64_t kd = dkv_k + static_cast<uint64_t>(slot * (kTileBytes >> 4));
+      const uint32_t hi = static_cast<uint32_t>(dq0 >> 32);
+      const uint32_t q_lo = static_cast<uint32_t>(dq0), k_lo = static_cast<uint32_t>(dkv_k),
+                     v_lo = static_cast<uint32_t>(dkv_v);
+      auto issue_qk = [&](int qb, int t, int slot) {
+        const uint32_t qd = q_lo + static_cast<uint32_t>((qb * kQTiles + t) * (kTileBytes >> 4));
+        const uint32_t kd = k_lo + static_cast<uint32_t>(slot * (kTileBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
-          umma_ss_elect(tmem + t * 128, qd + off, kd + off, idesc_s, kk > 0);
+          const uint32_t off = static_cast<uint32_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+          umma_ss_elect_lo(tmem + t * 128, qd + off, kd + off, hi, idesc_s, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint64_t vd = dkv_v + static_cast<uint64_t>(slot * (kTileBytes >> 4));
+        const uint32_t vd = v_lo + static_cast<uint32_t>(slot * (kTileBytes >> 4));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts_elect(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, vd + static_cast<uint64_t>(kk * (2048 >> 4)),
-                        idesc_o, (acc || kk > 0) ? 1u : 0u);
+          umma_ts_elect_lo(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, vd + static_cast<uint32_t>(kk * (2048 >> 4)),
+                           hi, idesc_o, (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = true;
-      for (int t = 0; t < kQTiles && ok; ++t) ok = warp_wait(&bar_q_ready[t], 0, abort, a.lc.err, to);
-      if (ok && n_tiles > 0) {
-        ok = warp_wait(&bar_kv_full[0], 0, abort, a.lc.err, to);
-        if (ok) {
-          tc_fence_after();
-          issue_qk(0, 0);
-          umma_commit_elect(&bar_s_full[0]);
-          issue_qk(1, 0);
-          umma_commit_elect(&bar_s_full[1]);
-          umma_commit_elect(&bar_kv_empty[0]);
-        }
-        for (int j = 0; j < n_tiles && ok; ++j) {
-          const int iv = 2 * j + 1;
+      int nq = 0;   // items with key tiles so far (Q buffer use)
+      int ig = 0;   // K/V ring position
+      int sp = 0;   // S/P phases so far (per tile)
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const Item x = item_of(it);
+        if (x.n_tiles == 0) continue;
+        const int qb = nq % kQBuf;
+        // Self-attention: the softmax warps rotate Q in shared memory first.
+        ok = warp_wait(kRope ? &bar_q_ready[qb] : &bar_q_full[qb], (nq / kQBuf) & 1, abort, a.lc.err, to);
+        if (!ok) break;
+        const int k0 = ig % kStages;
+        ok = warp_wait(&bar_kv_full[k0], (ig / kStages) & 1, abort, a.lc.err, to);
+        if (!ok) break;
+        tc_fence_after();
+        issue_qk(qb, 0, k0);
+        umma_commit_elect(&bar_s_full[0]);
+        issue_qk(qb, 1, k0);
+        umma_commit_elect(&bar_s_full[1]);
+        umma_commit_elect(&bar_kv_empty[k0]);
+        for (int j = 0; j < x.n_tiles && ok; ++j) {
+          const int iv = ig + 2 * j + 1;
           const int vslot = iv % kStages;
           ok = warp_wait(&bar_kv_full[vslot], (iv / kStages) & 1, abort, a.lc.err, to);
-          const bool has_next = j + 1 < n_tiles;
-          const int ik = 2 * j + 2;
+          const bool has_next = j + 1 < x.n_tiles;
+          const int ik = ig + 2 * j + 2;
           const int kslot = ik % kStages;
           if (ok && has_next) ok = warp_wait(&bar_kv_full[kslot], (ik / kStages) & 1, abort, a.lc.err, to);
           for (int t = 0; t < kQTiles && ok; ++t) {
-            ok = warp_wait(&bar_p_full[t], j & 1, abort, a.lc.err, to);
+            ok = warp_wait(&bar_p_full[t], (sp + j) & 1, abort, a.lc.err, to);
             if (!ok) break;
             tc_fence_after();
             issue_pv(t, vslot, j > 0);
@@ -252,18 +315,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!has_next) {
               umma_commit_elect(&bar_o_full[t]);
             } else {
-              issue_qk(t, kslot);
+              issue_qk(qb, t, kslot);
               umma_commit_elect(&bar_s_full[t]);
               if (t == kQTiles - 1) umma_commit_elect(&bar_kv_empty[kslot]);
             }
           }
         }
+        // All QK MMAs of this item are behind this commit: Q buffer qb is free.
+        umma_commit_elect(&bar_q_empty[qb]);
+        ig += 2 * x.n_tiles;
+        sp += x.n_tiles;
+        ++nq;
       }
       // Every MMA of this CTA must be done before TMEM is released.
       umma_commit_elect(&bar_drain);
       mbar_wait(&bar_drain, 0, nullptr, to);
     }
-    __syncwarp();
    }
   } else {
     regs_grow<kSoftmaxRegs>();
@@ -271,133 +338,159 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
-    const int row = q0 + t * kBlockM + r;
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_addr + t * 128;
     const uint32_t tO = tmem + lane_addr + 256 + t * 128;
     const float sl2 = a.scale_log2;
-
-    bool ok = warp_wait(&bar_q_full[t], 0, abort, a.lc.err, to);
-    if (kRope && ok && row < a.Lq) rope_row_in_smem(sQ + t * kTileBytes, r, row, a);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bar_q_ready[t]);
-
-    float m_ref = -INFINITY;
-    float l = 0.f;
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      ok = warp_wait(&bar_s_full[t], j & 1, abort, a.lc.err, to);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
-      tmem_ld_wait();
-#define WAN_S(e) __uint_as_float(sr[(e) >> 5][(e) & 31])
-      const int valid = n_valid - j * kBlockN;
-      if (valid < kBlockN) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i >= valid) sr[i >> 5][i & 31] = __float_as_uint(-INFINITY);
+    bool ok = true;
+    int nq = 0;  // items with key tiles so far
+    int sp = 0;  // S/P phases so far
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      // Only the key-tile counts stay live through the softmax loop; the
+      // output addresses are recomputed for the epilogue.
+      int n_valid, n_tiles, kv_start;
+      {
+        const Item x = item_of(it);
+        n_valid = x.n_valid;
+        n_tiles = x.n_tiles;
+        kv_start = x.kv_start;
       }
-      // Row max: four independent chains of three-input maxima.
-      float mc[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) mc[q] = WAN_S(q);
-#pragma unroll
-      for (int i = 4; i < 128; i += 8) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          mc[q] = max3f(mc[q], WAN_S(i + 2 * q), WAN_S(i + 2 * q + 1));
-      }
-      const float mx = max3f(mc[0], mc[1], fmaxf(mc[2], mc[3]));
-      const float m_new = fmaxf(m_ref, mx);
-      if (j == 0) {
-        m_ref = m_new;
-      } else {
-        const bool need = (m_new - m_ref) * sl2 > kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? ex2_approx((m_ref - m_new) * sl2) : 1.0f;
-          if (need) {
-            l *= alpha;
-            m_ref = m_new;
-          }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tO + c * 32, ov);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(tO + c * 32, ov);
-          }
+      if (n_tiles == 0) {  // no valid key: O = 0, LSE = -inf
+        const Item x = item_of(it);
+        const int row = x.q0 + t * kBlockM + r;
+        if (row < a.Lq) {
+          uint4* dst = reinterpret_cast<uint4*>(a.o + ((static_cast<size_t>(x.b) * a.Lq + row) * a.H + x.h) * kHeadDim);
+          for (int c = 0; c < 16; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+          if (a.lse) a.lse[(static_cast<size_t>(x.b) * a.H + x.h) * a.Lq + row] = -INFINITY;
         }
+        continue;
       }
-      // p = 2^(s * scale * log2(e) - m * scale * log2(e)), two lanes per f32x2 op.
-      const float neg = -m_ref * sl2;
-      const uint64_t sl2x2 = f2_pack(sl2, sl2);
-      const uint64_t negx2 = f2_pack(neg, neg);
-      uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int e = c * 32 + 2 * i;
-          const uint64_t x = f2_fma(f2_pack(WAN_S(e), WAN_S(e + 1)), sl2x2, negx2);
-          float x0, x1;
-          f2_unpack(x, x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          const uint64_t pp = f2_pack(p0, p1);
-          acc[i & 1] = f2_add(acc[i & 1], pp);
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tS + c * 16, pk);
+      const int qb = nq % kQBuf;
+      if (kRope) {
+        ok = warp_wait(&bar_q_full[qb], (nq / kQBuf) & 1, abort, a.lc.err, to);
+        if (!ok) break;
+        const int row = item_of(it).q0 + t * kBlockM + r;
+        if (row < a.Lq) rope_row_in_smem(sQ + (qb * kQTiles + t) * kTileBytes, r, row, a);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_q_ready[qb]);
       }
-      float a0, a1, a2, a3;
-      f2_unpack(acc[0], a0, a1);
-      f2_unpack(acc[1], a2, a3);
-      const float lsum = (a0 + a1) + (a2 + a3);
-#undef WAN_S
-      l += lsum;
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_p_full[t]);
-    }
 
-    // ------------------------------------------------------------ epilogue
-    __nv_bfloat16* orow = a.o + ((static_cast<size_t>(b) * a.Lq + row) * a.H + h) * kHeadDim;
-    if (n_tiles == 0) {
-      if (row < a.Lq) {
-        uint4* dst = reinterpret_cast<uint4*>(orow);
-        for (int c = 0; c < 16; ++c) dst[c] = make_uint4(0, 0, 0, 0);
-        if (a.lse) a.lse[(static_cast<size_t>(b) * a.H + h) * a.Lq + row] = -INFINITY;
-      }
-    } else if (ok) {
-      ok = warp_wait(&bar_o_full[t], 0, abort, a.lc.err, to);
-      if (ok) {
+      float m_ref = -INFINITY;
+      float l = 0.f;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        ok = warp_wait(&bar_s_full[t], (sp + j) & 1, abort, a.lc.err, to);
+        if (!ok) break;
         tc_fence_after();
-        const float inv = 1.0f / l;
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
+        tmem_ld_wait();
+#define WAN_S(e) __uint_as_float(sr[(e) >> 5][(e) & 31])
+        const int jt = j + kv_start < n_tiles ? j + kv_start : j + kv_start - n_tiles;
+        const int valid = n_valid - jt * kBlockN;
+        if (valid < kBlockN) {
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i >= valid) sr[i >> 5][i & 31] = __float_as_uint(-INFINITY);
+        }
+        // Row max: four independent chains of three-input maxima.
+        float mc[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mc[q] = WAN_S(q);
+#pragma unroll
+        for (int i = 4; i < 128; i += 8) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            mc[q] = max3f(mc[q], WAN_S(i + 2 * q), WAN_S(i + 2 * q + 1));
+        }
+        const float mx = max3f(mc[0], mc[1], fmaxf(mc[2], mc[3]));
+        const float m_new = fmaxf(m_ref, mx);
+        if (j == 0) {
+          m_ref = m_new;
+        } else {
+          const bool need = (m_new - m_ref) * sl2 > kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ex2_approx((m_ref - m_new) * sl2) : 1.0f;
+            if (need) {
+              l *= alpha;
+              m_ref = m_new;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t ov[32];
+              tmem_ld32(tO + c * 32, ov);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+              tmem_st32(tO + c * 32, ov);
+            }
+          }
+        }
+        // p = 2^(s * scale * log2(e) - m * scale * log2(e)), two lanes per f32x2 op.
+        const float neg = -m_ref * sl2;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        const uint64_t negx2 = f2_pack(neg, neg);
+        uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(tO + c * 32, ov);
-          tmem_ld_wait();
           uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
-          if (row < a.Lq) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int i = 0; i < 16; ++i) {
+            const int e = c * 32 + 2 * i;
+            const uint64_t xx = f2_fma(f2_pack(WAN_S(e), WAN_S(e + 1)), sl2x2, negx2);
+            float x0, x1;
+            f2_unpack(xx, x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            const uint64_t pp = f2_pack(p0, p1);
+            acc[i & 1] = f2_add(acc[i & 1], pp);
+            pk[i] = pack_bf16x2(p0, p1);
           }
+          tmem_st16(tS + c * 16, pk);
         }
-        if (a.lse && row < a.Lq)
-          a.lse[(static_cast<size_t>(b) * a.H + h) * a.Lq + row] = (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f;
+        float a0, a1, a2, a3;
+        f2_unpack(acc[0], a0, a1);
+        f2_unpack(acc[1], a2, a3);
+        const float lsum = (a0 + a1) + (a2 + a3);
+#undef WAN_S
+        l += lsum;
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_p_full[t]);
       }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- epilogue
+      ok = warp_wait(&bar_o_full[t], nq & 1, abort, a.lc.err, to);
+      if (!ok) break;
+      tc_fence_after();
+      const Item x = item_of(it);
+      const int row = x.q0 + t * kBlockM + r;
+      __nv_bfloat16* orow = a.o + ((static_cast<size_t>(x.b) * a.Lq + row) * a.H + x.h) * kHeadDim;
+      float* lse_p = a.lse ? a.lse + (static_cast<size_t>(x.b) * a.H + x.h) * a.Lq + row : nullptr;
+      const float inv = 1.0f / l;
+      // O_t is read out of TMEM here; the next item's first PV overwrites it
+      // only after this warp signals that item's first P (program order).
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tO + c * 32, ov);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
+        if (row < a.Lq) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+      if (lse_p && row < a.Lq) *lse_p = (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f;
+      sp += n_tiles;
+      ++nq;
     }
   }
 
@@ -426,16 +519,25 @@ int launch_attn_fwd(const void* q, const void* k_rot, const void* v, void* o, fl
   a.Lq = Lq;
   a.Lk = Lk;
   a.H = H;
+  a.B = B;
   a.Hp = g.Hp;
   a.Wp = g.Wp;
+  a.n_qpairs = (Lq + kBlockM * kQTiles - 1) / (kBlockM * kQTiles);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.lc = lc;
-  dim3 grid((Lq + kBlockM * kQTiles - 1) / (kBlockM * kQTiles), H, B);
+  const long long n_items = static_cast<long long>(a.n_qpairs) * H * B;
+  if (n_items > INT_MAX) return WAN_ERR_INVALID;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return WAN_ERR_CUDA;
+  const int grid = static_cast<int>(n_items < sms ? n_items : sms);  // persistent: one CTA per SM
   auto kern = rope ? attn_fwd_kernel<true> : attn_fwd_kernel<false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+  const int smem_bytes = rope ? FwdCfg<true>::kSmemBytes : FwdCfg<false>::kSmemBytes;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
     return WAN_ERR_CUDA;
   record_start(lc, s);
-  kern<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, a);
+  kern<<<grid, kThreads, smem_bytes, s>>>(tq, tk, tv, a);
   record_stop(lc, s);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
