@@ -15,9 +15,10 @@
 // Three warpgroups (register budgets moved with setmaxnreg):
 //   warps 0-3   softmax of query tile 0 (one thread per row)      208 regs
 //   warps 4-7   softmax of query tile 1                           208 regs
-//   warp  8     TMA producer (Q per item, then K_j, V_j into a ring)
+//   warp  8     TMA producer of K_j, V_j (ring)
 //   warp  9     MMA issuer (warp-converged, one elected lane) and TMEM owner
-//   warps 10-11 idle                                               88 regs
+//   warp  10    TMA producer of the items' Q tiles
+//   warp  11    idle                                               88 regs
 // Cross-attention items are short (at most 4 key tiles), so there Q is
 // double-buffered: the next item's Q load and first QK overlap the current
 // item's output epilogue. Self-attention uses one Q buffer and a 4-slot ring.
@@ -54,6 +55,7 @@ constexpr uint32_t kSoftmaxRegs = 208;  // 2 x 128 x 208 + 128 x 88 = 384 x 168
 constexpr uint32_t kControlRegs = 88;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kQLoadWarp = 10;
 // Q buffers and K/V ring slots (self-attention: 1 + 4, cross-attention: 2 + 3).
 template <bool kRope>
 struct FwdCfg {
@@ -198,27 +200,13 @@ __global__ void __launch_bounds__(kThreads, 1)
    if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int nq = 0;  // items whose Q was loaded
       int ig = 0;  // K/V tiles issued (ring position)
       bool ok = true;
       for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
         const Item x = item_of(it);
         if (x.n_tiles == 0) continue;
-        const int qb = nq % kQBuf;
-        if (nq >= kQBuf && !mbar_wait(&bar_q_empty[qb], ((nq / kQBuf) - 1) & 1, abort, to)) {
-          raise_abort(abort, a.lc.err);
-          break;
-        }
-        uint8_t* qdst = sQ + qb * (kQTiles * kTileBytes);
-        mbar_arrive_expect_tx(&bar_q_full[qb], kQTiles * kTileBytes);
-        for (int t = 0; t < kQTiles; ++t) {
-          tma_load_4d(qdst + t * kTileBytes, &tm_q, &bar_q_full[qb], 0, x.h, x.q0 + t * kBlockM, x.b);
-          tma_load_4d(qdst + t * kTileBytes + kHalfBytes, &tm_q, &bar_q_full[qb], 64, x.h, x.q0 + t * kBlockM, x.b);
-        }
-        ++nq;
         for (int i = 0; i < 2 * x.n_tiles; ++i, ++ig) {
           const int slot = ig % kStages;
           const int use = ig / kStages;
@@ -242,6 +230,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       // fill of each slot / buffer is that barrier's latest phase.
       for (int k = ig - kStages < 0 ? 0 : ig - kStages; k < ig; ++k)
         mbar_wait(&bar_kv_full[k % kStages], (k / kStages) & 1, nullptr, to);
+    }
+    __syncwarp();
+   } else if (warp == kQLoadWarp) {
+    // ------------------------------------------------------------ Q producer
+    // Q tiles of each item go into their buffer as soon as it is free, so a
+    // Q prefetch never waits behind the K/V ring.
+    if (lane == 0) {
+      int nq = 0;  // items whose Q was loaded
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const Item x = item_of(it);
+        if (x.n_tiles == 0) continue;
+        const int qb = nq % kQBuf;
+        if (nq >= kQBuf && !mbar_wait(&bar_q_empty[qb], ((nq / kQBuf) - 1) & 1, abort, to)) {
+          raise_abort(abort, a.lc.err);
+          break;
+        }
+        uint8_t* qdst = sQ + qb * (kQTiles * kTileBytes);
+        mbar_arrive_expect_tx(&bar_q_full[qb], kQTiles * kTileBytes);
+        for (int t = 0; t < kQTiles; ++t) {
+          tma_load_4d(qdst + t * kTileBytes, &tm_q, &bar_q_full[qb], 0, x.h, x.q0 + t * kBlockM, x.b);
+          tma_load_4d(qdst + t * kTileBytes + kHalfBytes, &tm_q, &bar_q_full[qb], 64, x.h, x.q0 + t * kBlockM, x.b);
+        }
+        ++nq;
+      }
+      // Every Q copy lands before the CTA may exit.
       for (int k = nq - kQBuf < 0 ? 0 : nq - kQBuf; k < nq; ++k)
         mbar_wait(&bar_q_full[k % kQBuf], (k / kQBuf) & 1, nullptr, to);
     }
