@@ -13,12 +13,12 @@
 // Persistent CTAs (one per SM) walk a static list of work items; an item is
 // 2 query tiles of 128 rows of one (b, h), processed against all key tiles.
 // Three warpgroups (register budgets moved with setmaxnreg):
-//   warps 0-3   softmax of query tile 0 (one thread per row)      208 regs
-//   warps 4-7   softmax of query tile 1                           208 regs
+//   warps 0-3   softmax of query tile 0 (one thread per row)      216 regs
+//   warps 4-7   softmax of query tile 1                           216 regs
 //   warp  8     TMA producer of K_j, V_j (ring)
 //   warp  9     MMA issuer (warp-converged, one elected lane) and TMEM owner
 //   warp  10    TMA producer of the items' Q tiles
-//   warp  11    idle                                               88 regs
+//   warp  11    idle                                               72 regs
 // Cross-attention items are short (at most 4 key tiles), so there Q is
 // double-buffered: the next item's Q load and first QK overlap the current
 // item's output epilogue. Self-attention uses one Q buffer and a 4-slot ring.
@@ -51,8 +51,8 @@ constexpr int kBlockN = 128;
 constexpr int kTileBytes = 128 * 128 * 2;
 constexpr int kHalfBytes = kTileBytes / 2;
 constexpr int kThreads = 384;
-constexpr uint32_t kSoftmaxRegs = 208;  // 2 x 128 x 208 + 128 x 88 = 384 x 168
-constexpr uint32_t kControlRegs = 88;
+constexpr uint32_t kSoftmaxRegs = 216;  // 2 x 128 x 216 + 128 x 72 = 384 x 168
+constexpr uint32_t kControlRegs = 72;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kQLoadWarp = 10;
@@ -121,7 +121,8 @@ __device__ __forceinline__ void rope_row_in_smem(uint8_t* tile, int r, int row, 
 template <bool kRope>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const FwdArgs a) {
   constexpr int kQBuf = FwdCfg<kRope>::kQBuf;
   constexpr int kStages = FwdCfg<kRope>::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t bar_drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
+  __shared__ int epi_ok[kQTiles][4];  // per-warp epilogue go/stop flags
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -171,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int q = 0; q < kQBuf; ++q) {
       mbar_init(&bar_q_full[q], 1);
       mbar_init(&bar_q_ready[q], kRope ? 8 : 1);
-      mbar_init(&bar_q_empty[q], 1);
+      mbar_init(&bar_q_empty[q], kQTiles);  // one arrive per query tile, after its O store
     }
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(&bar_s_full[t], 1);
@@ -334,8 +336,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        // All QK MMAs of this item are behind this commit: Q buffer qb is free.
-        umma_commit_elect(&bar_q_empty[qb]);
         ig += 2 * x.n_tiles;
         sp += x.n_tiles;
         ++nq;
@@ -476,13 +476,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // ---------------------------------------------------------- epilogue
+      // O_t is normalised into bf16 and staged in this tile's Q buffer (no
+      // MMA reads it once O_t is final) in the 128-byte swizzled layout, then
+      // one thread writes it with two TMA tensor stores and, once they have
+      // read the staging area, hands the buffer back to the Q producer. The
+      // four warps of the tile agree on stopping before the named barriers.
       ok = warp_wait(&bar_o_full[t], nq & 1, abort, a.lc.err, to);
-      if (!ok) break;
+      if (lane == 0) epi_ok[t][wq] = ok ? 1 : 0;
+      named_bar_sync(1 + t, 128);
+      if (!(epi_ok[t][0] & epi_ok[t][1] & epi_ok[t][2] & epi_ok[t][3])) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const Item x = item_of(it);
       const int row = x.q0 + t * kBlockM + r;
-      __nv_bfloat16* orow = a.o + ((static_cast<size_t>(x.b) * a.Lq + row) * a.H + x.h) * kHeadDim;
-      float* lse_p = a.lse ? a.lse + (static_cast<size_t>(x.b) * a.H + x.h) * a.Lq + row : nullptr;
+      uint8_t* stage = sQ + (qb * kQTiles + t) * kTileBytes;
       const float inv = 1.0f / l;
       // O_t is read out of TMEM here; the next item's first PV overwrites it
       // only after this warp signals that item's first P (program order).
@@ -491,22 +500,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ov[32];
         tmem_ld32(tO + c * 32, ov);
         tmem_ld_wait();
-        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
-        if (row < a.Lq) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        for (int q = 0; q < 4; ++q) {  // 16-byte chunk 4c+q of the row: half c/2, chunk (4c+q)%8
+          uint32_t pk[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int i = 0; i < 4; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(ov[8 * q + 2 * i]) * inv, __uint_as_float(ov[8 * q + 2 * i + 1]) * inv);
+          const int chunk = 4 * c + q;
+          *reinterpret_cast<uint4*>(stage + (chunk >> 3) * kHalfBytes + sw128_offset(r, chunk & 7)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
-      if (lse_p && row < a.Lq) *lse_p = (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f;
+      if (a.lse && row < a.Lq)
+        a.lse[(static_cast<size_t>(x.b) * a.H + x.h) * a.Lq + row] = (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f;
+      fence_proxy_async_smem();
+      named_bar_sync(1 + t, 128);
+      if (wq == 0 && lane == 0) {
+        // Rows past the end of the sequence fall outside the tensor map and
+        // are not written.
+        tma_store_4d(&tm_o, stage, 0, x.h, x.q0 + t * kBlockM, x.b);
+        tma_store_4d(&tm_o, stage + kHalfBytes, 64, x.h, x.q0 + t * kBlockM, x.b);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(&bar_q_empty[qb]);
+      }
       sp += n_tiles;
       ++nq;
     }
   }
 
+  // The O stores still in flight finish before the kernel's writes become
+  // visible; only their reads of shared memory must end before exit.
+  if (warp == 0 || warp == 4) bulk_wait_group0();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -520,8 +545,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 int launch_attn_fwd(const void* q, const void* k_rot, const void* v, void* o, float* lse, int B, int Lq, int Lk,
                     int H, wan_grid_t g, RopeTables tab, bool rope, const int32_t* kv_lens, float scale,
                     const LaunchCommon& lc, cudaStream_t s) {
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!make_tmap_bld(&tq, q, B, Lq, H, kHeadDim, 128)) return WAN_ERR_CUDA;
+  if (!make_tmap_bld(&to, o, B, Lq, H, kHeadDim, 128)) return WAN_ERR_CUDA;
   if (!make_tmap_bld(&tk, k_rot, B, Lk, H, kHeadDim, 128)) return WAN_ERR_CUDA;
   if (!make_tmap_bld(&tv, v, B, Lk, H, kHeadDim, 128)) return WAN_ERR_CUDA;
   FwdArgs a;
@@ -550,7 +576,7 @@ int launch_attn_fwd(const void* q, const void* k_rot, const void* v, void* o, fl
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
     return WAN_ERR_CUDA;
   record_start(lc, s);
-  kern<<<grid, kThreads, smem_bytes, s>>>(tq, tk, tv, a);
+  kern<<<grid, kThreads, smem_bytes, s>>>(tq, tk, tv, to, a);
   record_stop(lc, s);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
