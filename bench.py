@@ -165,6 +165,112 @@ def timing_pairs(torch, stream, n):
     return pairs
 
 
+class Case:
+    """One workload as the bench runs it: the timed step, its FLOP count, the
+    dominant kernel the roofline describes, and the end-to-end variant that
+    moves the step's inputs and results through pinned host memory."""
+
+
+def make_case(wan, torch, dev, w, rank, peaks):
+    B, L, H, d, grid = w.B, w.L, w.H, w.d, w.grid
+    scale = 1.0 / math.sqrt(d)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + rank)
+    stream = torch.cuda.current_stream(dev)
+    c = Case()
+    c.stream = stream
+    fwd_flops = 4.0 * B * H * L * (w.Lk if w.kind == "cross_fwd" else L) * d
+    if w.kind == "cross_fwd":
+        from long_sequence_attention_02_b300 import synth
+
+        Lk = w.Lk
+        q = torch.randn(B, L, H, d, device=dev, generator=gen).bfloat16()
+        k = torch.randn(B, Lk, H, d, device=dev, generator=gen).bfloat16()
+        v = torch.randn(B, Lk, H, d, device=dev, generator=gen).bfloat16()
+        lens_np = synth.kv_lens(0, B)
+        lens = torch.from_numpy(lens_np).to(dev)
+        o, lse = torch.empty_like(q), torch.empty(B, H, L, device=dev)
+
+        def run():
+            wan.check(wan.wan_xattn_fwd(q, k, v, lens, Lk, o, lse, B, grid, H, d, scale, stream))
+
+        c.inputs, c.outputs = [q, k, v], [o, lse]
+        c.flops, c.kernel, c.kernel_flops, c.launches = fwd_flops, "attn_fwd_kernel<false>", fwd_flops, 1
+        c.extra_config = {"Lk": Lk, "kv_lens": lens_np.tolist(),
+                          "useful_flop_per_step": 4.0 * H * L * d * float(lens_np.sum())}
+        # HBM roofline: Q read + O written once, LSE written, K/V read once.
+        c.hbm_bytes = q.numel() * 2 * 2 + lse.numel() * 4 + 2 * k.numel() * 2
+        c.bound = "hbm"
+    else:
+        q = torch.randn(B, L, H, d, device=dev, generator=gen).bfloat16()
+        k = torch.randn(B, L, H, d, device=dev, generator=gen).bfloat16()
+        v = torch.randn(B, L, H, d, device=dev, generator=gen).bfloat16()
+        o, lse = torch.empty_like(q), torch.empty(B, H, L, device=dev)
+        tables = wan.rope_tables(grid, device=dev)
+        wsf = wan.wan_attn_workspace_size(wan.WAN_OP_FWD, B, grid, H, d)
+        if w.kind == "self_fwd":
+            ws = torch.empty(wsf, dtype=torch.uint8, device=dev)
+
+            def run():
+                wan.check(wan.wan_attn_fwd(q, k, v, o, lse, B, grid, H, d, tables, scale, ws, wsf, stream))
+
+            c.inputs, c.outputs = [q, k, v], [o, lse]
+            c.flops, c.kernel, c.kernel_flops, c.launches = fwd_flops, "attn_fwd_kernel<true>", fwd_flops, 2
+            c.hbm_bytes = None
+            c.bound = "tensor"
+        else:  # forward + backward (one training step of the attention)
+            do = torch.randn(B, L, H, d, device=dev, generator=gen).bfloat16()
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+            wsb = wan.wan_attn_workspace_size(wan.WAN_OP_BWD, B, grid, H, d)
+            ws = torch.empty(max(wsf, wsb), dtype=torch.uint8, device=dev)
+            pad = 1 if L % 128 else 0
+            state = {"prof": None}
+
+            def run():
+                wan.check(wan.wan_attn_fwd(q, k, v, o, lse, B, grid, H, d, tables, scale, ws, wsf, stream))
+                if state["prof"] is not None:
+                    wan.check(wan.wan_profile_set_events(*state["prof"]))
+                wan.check(wan.wan_attn_bwd(q, k, v, o, lse, do, dq, dk, dv, B, grid, H, d, tables, scale, ws, wsb,
+                                           stream))
+
+            c.state = state
+            c.inputs, c.outputs = [q, k, v, do], [dq, dk, dv]
+            c.flops = 3.5 * fwd_flops
+            c.kernel, c.kernel_flops = "attn_bwd_kernel", 2.5 * fwd_flops
+            # forward: K rotation + attention; backward: Q and K rotation, row
+            # pass (+ padding), attention backward, dQ rotation back
+            c.launches = 2 + 5 + pad
+            c.hbm_bytes = None
+            c.bound = "tensor"
+
+    def step(prof=None):
+        if hasattr(c, "state"):
+            c.state["prof"] = prof
+        elif prof is not None:
+            wan.check(wan.wan_profile_set_events(*prof))
+        run()
+
+    c.step = step
+    c.in_bytes = sum(t.numel() * t.element_size() for t in c.inputs)
+    c.out_bytes = sum(t.numel() * t.element_size() for t in c.outputs)
+    return c
+
+
+def read_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` recorded under profiles/ for this
+    workload, or None if absent or taken from a different kernel source."""
+    prof_path = os.path.join(HERE, "profiles", "traffic.json")
+    try:
+        with open(prof_path) as f:
+            tr = json.load(f)
+    except Exception:
+        return None
+    ent = tr.get(kernel, {})
+    if ent.get("source_fingerprint") != source_fingerprint(kernel) or ent.get("workload") not in (None, workload):
+        return None
+    return ent.get("bytes_per_launch")
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -175,29 +281,11 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     peaks = _peaks()
     w = WORKLOADS[args.workload]
-    B, L, H, d, grid = w.B, w.L, w.H, w.d, w.grid
-    flops = 4.0 * B * H * L * L * d
-    scale = 1.0 / math.sqrt(d)
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(1000 + rank)
-    q = torch.randn(B, L, H, d, device=dev, generator=gen).bfloat16()
-    k = torch.randn(B, L, H, d, device=dev, generator=gen).bfloat16()
-    v = torch.randn(B, L, H, d, device=dev, generator=gen).bfloat16()
-    o = torch.empty_like(q)
-    lse = torch.empty(B, H, L, device=dev)
-    tables = wan.rope_tables(grid, device=dev)
-    ws_bytes = wan.wan_attn_workspace_size(wan.WAN_OP_FWD, B, grid, H, d)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    in_bytes = 3 * q.numel() * 2
-
-    def step(prof=None):
-        if prof is not None:
-            wan.check(wan.wan_profile_set_events(*prof))
-        wan.check(wan.wan_attn_fwd(q, k, v, o, lse, B, grid, H, d, tables, scale, ws, ws_bytes, stream))
+    c = make_case(wan, torch, dev, w, rank, peaks)
+    stream = c.stream
 
     for _ in range(args.warmup):
-        step()
+        c.step()
     torch.cuda.synchronize()
     wan.check(wan.wan_get_device_status())
 
@@ -210,7 +298,7 @@ def run_ours(args, rank, world, local):
     time.sleep(0.3)
     e0.record(stream)
     for i in range(args.steps):
-        step(kev[i])
+        c.step(kev[i])
     e1.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -219,23 +307,18 @@ def run_ours(args, rank, world, local):
     ms = e0.elapsed_time(e1) / args.steps
     kernel_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
     ms_max = max_over_ranks(ms, world)
-    value = aggregate(flops, world, ms_max / 1e3) / 1e12
-    kernel_tflops = flops / (kernel_ms / 1e3) / 1e12
+    value = aggregate(c.flops, world, ms_max / 1e3) / 1e12
 
     # ----- end to end through the C ABI with host buffers
-    qh = q.cpu().pin_memory()
-    kh = k.cpu().pin_memory()
-    vh = v.cpu().pin_memory()
-    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    lseh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    hin = [t.cpu().pin_memory() for t in c.inputs]
+    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in c.outputs]
 
     def e2e_step():
-        q.copy_(qh, non_blocking=True)
-        k.copy_(kh, non_blocking=True)
-        v.copy_(vh, non_blocking=True)
-        wan.check(wan.wan_attn_fwd(q, k, v, o, lse, B, grid, H, d, tables, scale, ws, ws_bytes, stream))
-        oh.copy_(o, non_blocking=True)
-        lseh.copy_(lse, non_blocking=True)
+        for dst, src in zip(c.inputs, hin):
+            dst.copy_(src, non_blocking=True)
+        c.step()
+        for dst, src in zip(hout, c.outputs):
+            dst.copy_(src, non_blocking=True)
 
     e2e_steps = max(1, min(args.steps, 5))
     e2e_step()
@@ -248,27 +331,38 @@ def run_ours(args, rank, world, local):
     a1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a0.elapsed_time(a1) / e2e_steps, world)
-    e2e = {"value": round(aggregate(flops, world, e2e_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
-           "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
-           "ms_per_step": round(e2e_ms, 3)}
-    del qh, kh, vh, oh, lseh
+    e2e = {"value": round(aggregate(c.flops, world, e2e_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": c.in_bytes, "d2h_bytes_per_step": c.out_bytes, "ms_per_step": round(e2e_ms, 3)}
+    del hin, hout
 
     also = {}
     if not args.no_extras and rank == 0:
-        also = extras(wan, torch, dev, peaks)
+        also = extras(wan, torch, dev, peaks, skip=w.name)
 
-    peak = peaks["bf16_tflops_sustained"]
-    traffic = None
-    prof_path = os.path.join(HERE, "profiles", "traffic.json")
-    if os.path.exists(prof_path):
-        try:
-            with open(prof_path) as f:
-                tr = json.load(f)
-            ent = tr.get("attn_fwd_kernel", {})
-            if ent.get("source_fingerprint") == source_fingerprint():
-                traffic = ent.get("bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = read_traffic(c.kernel, w.name)
+    if c.bound == "tensor":
+        peak = peaks["bf16_tflops_sustained"]
+        achieved = c.kernel_flops / (kernel_ms / 1e3) / 1e12
+        roofline = {"bound": "tensor", "kernel": c.kernel, "achieved": round(achieved, 2), "peak": peak,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "peak_kind": f"bf16 sustained ({peaks['source']})",
+                    "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4),
+                    "frac_of_2.25PF_spec": round(achieved / 2250.0, 4),
+                    "kernel_ms": round(kernel_ms, 3), "traffic": traffic}
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = c.hbm_bytes / (kernel_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm", "kernel": c.kernel, "achieved": round(achieved, 1), "peak": peak,
+                    "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"HBM copy ({peaks['source']})",
+                    "algorithmic_bytes": c.hbm_bytes, "kernel_ms": round(kernel_ms, 3), "traffic": traffic,
+                    "tensor_tflops_nominal": round(c.kernel_flops / (kernel_ms / 1e3) / 1e12, 2)}
+    config = {"workload": w.name, "kind": w.kind, "B": w.B, "grid": list(w.grid), "tokens": w.L, "heads": w.H,
+              "head_dim": w.d, "flop_per_step": c.flops,
+              "l2": f"inputs {c.in_bytes / 2**30:.2f} GiB > L2 126 MB (no flush needed)",
+              "frac_of_2.25PF_spec": round(value / 2250.0, 4)}
+    if w.kind != "cross_fwd":
+        config["theta"] = 10000.0
+    config.update(getattr(c, "extra_config", {}))
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -281,19 +375,12 @@ def run_ours(args, rank, world, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
-        "data": "synthetic: bf16 N(0,1) Q, K, V (torch generator, seed 1000+rank)",
-        "config": {"workload": w.name, "B": B, "grid": list(grid), "tokens": L, "heads": H, "head_dim": d,
-                   "theta": 10000.0, "flop_per_step": flops,
-                   "l2": f"inputs {in_bytes / 2**30:.2f} GiB > L2 126 MB (no flush needed)",
-                   "frac_of_2.25PF_spec": round(value / 2250.0, 4)},
-        "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel", "achieved": round(kernel_tflops, 2),
-                     "peak": peak, "unit": "TFLOP/s", "frac": round(kernel_tflops / peak, 4),
-                     "peak_kind": f"bf16 sustained ({peaks['source']})",
-                     "frac_of_burst": round(kernel_tflops / peaks["bf16_tflops"], 4),
-                     "kernel_ms": round(kernel_ms, 3), "traffic": traffic},
+        "data": "synthetic: bf16 N(0,1) inputs (torch generator, seed 1000+rank)",
+        "config": config,
+        "roofline": roofline,
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": c.launches * args.steps,
     }
     if also:
         line["also"] = also
@@ -303,7 +390,7 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
-def extras(wan, torch, dev, peaks):
+def extras(wan, torch, dev, peaks, skip=None):
     """Secondary workloads, each timed with CUDA events (3 iterations after 2 warm-ups)."""
     from long_sequence_attention_02_b300.workloads import WORKLOADS
 
@@ -328,6 +415,20 @@ def extras(wan, torch, dev, peaks):
 
     # 480p self-attention forward
     w = WORKLOADS["wan1.3b_480p_self_fwd"]
+    if w.name == skip:
+        w = None
+    if w is not None:
+        _extra_480p(wan, torch, dev, w, stream, timeit, out)
+    w = WORKLOADS["wan14b_720p_cross_fwd"]
+    if w.name != skip:
+        _extra_cross(wan, torch, dev, w, stream, timeit, out, peaks)
+    w = WORKLOADS["train_64x64x64_fwd_bwd"]
+    if w.name != skip:
+        _extra_train(wan, torch, dev, w, stream, timeit, out)
+    return out
+
+
+def _extra_480p(wan, torch, dev, w, stream, timeit, out):
     B, L, H, d = w.B, w.L, w.H, w.d
     q = torch.randn(B, L, H, d, device=dev).bfloat16()
     k, v = torch.randn_like(q), torch.randn_like(q)
@@ -346,8 +447,8 @@ def extras(wan, torch, dev, peaks):
     out[w.name] = {"ms": round(tot, 3), "tflops": round(fl / tot / 1e9, 1), "kernel_tflops": round(fl / ker / 1e9, 1)}
     del q, k, v, o, lse, ws
 
-    # cross-attention forward
-    w = WORKLOADS["wan14b_720p_cross_fwd"]
+
+def _extra_cross(wan, torch, dev, w, stream, timeit, out, peaks):
     B, Lq, H, d, Lk = w.B, w.L, w.H, w.d, w.Lk
     q = torch.randn(B, Lq, H, d, device=dev).bfloat16()
     k = torch.randn(B, Lk, H, d, device=dev).bfloat16()
@@ -372,8 +473,8 @@ def extras(wan, torch, dev, peaks):
                    "gbs": round(hbm / tot / 1e6, 1), "hbm_frac": round(hbm / tot / 1e6 / peaks["hbm_gbs"], 3)}
     del q, k, v, o, lse
 
-    # training step: forward + backward at 64^3 tokens
-    w = WORKLOADS["train_64x64x64_fwd_bwd"]
+
+def _extra_train(wan, torch, dev, w, stream, timeit, out):
     B, L, H, d = w.B, w.L, w.H, w.d
     q = torch.randn(B, L, H, d, device=dev).bfloat16()
     k, v, do = torch.randn_like(q), torch.randn_like(q), torch.randn_like(q)
@@ -404,52 +505,71 @@ def extras(wan, torch, dev, peaks):
                    "tflops_bwd_kernel": round(2.5 * ffl / ker_b / 1e9, 1),
                    "tflops_bwd": round(2.5 * ffl / (tot - tot_f) / 1e9, 1),
                    "tflops_step": round(3.5 * ffl / tot / 1e9, 1)}
-    return out
 
 
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline leg and reference arm)
 
 
-def source_fingerprint() -> str:
+KERNEL_SOURCES = {
+    "attn_fwd_kernel<true>": ("attn_fwd.cu", "common.cuh"),
+    "attn_fwd_kernel<false>": ("attn_fwd.cu", "common.cuh"),
+    "attn_bwd_kernel": ("attn_bwd.cu", "common.cuh"),
+}
+
+
+def source_fingerprint(kernel: str = "attn_fwd_kernel<true>") -> str:
     import hashlib
 
     h = hashlib.sha1()
-    for name in ("attn_fwd.cu", "common.cuh"):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(HERE, "long_sequence_attention_02_b300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:12]
 
 
 def _oracle_rows(w, rows_per_head: int, heads: int, seed: int = 0):
-    """Time the oracle on `rows_per_head` query rows of `heads` heads."""
+    """Time the oracle on `rows_per_head` query rows of `heads` heads.
+
+    Self-attention rows run the oracle's 3D-RoPE forward (and, for a training
+    workload, its dQ backward too); cross-attention rows attend to the valid
+    text keys of batch 0. Returns (rows, seconds, convention FLOP per row).
+    """
     import numpy as np
 
     from long_sequence_attention_02_b300 import synth
     from oracle import ref
 
-    L, d = w.L, w.d
-    H = w.H
+    L, d, H = w.L, w.d, w.H
+    Lk = w.Lk if w.kind == "cross_fwd" else L
     t0 = time.perf_counter()
     n = 0
     for h in range(heads):
-        idx_k = (np.arange(L, dtype=np.uint64)[:, None] * H + h) * d + np.arange(d, dtype=np.uint64)[None, :]
+        idx_k = (np.arange(Lk, dtype=np.uint64)[:, None] * H + h) * d + np.arange(d, dtype=np.uint64)[None, :]
         kh = synth.bf16_bits_to_f64(synth.normal_bf16_at(seed, synth.STREAM_K, idx_k))
         vh = synth.bf16_bits_to_f64(synth.normal_bf16_at(seed, synth.STREAM_V, idx_k))
         rows = np.arange(rows_per_head, dtype=np.int64) * (L // rows_per_head)
         idx_q = (rows.astype(np.uint64)[:, None] * H + h) * d + np.arange(d, dtype=np.uint64)[None, :]
         qr = synth.bf16_bits_to_f64(synth.normal_bf16_at(seed, synth.STREAM_Q, idx_q))
-        ref.self_attention_fwd_rows(qr, rows, kh, vh, w.grid)
+        if w.kind == "cross_fwd":
+            ref.softmax_attention(qr, kh, vh, 1.0 / math.sqrt(d), int(synth.kv_lens(seed, w.B)[0]))
+        else:
+            ref.self_attention_fwd_rows(qr, rows, kh, vh, w.grid)
+            if w.kind == "self_fwd_bwd":
+                dor = synth.bf16_bits_to_f64(synth.normal_bf16_at(seed, synth.STREAM_DO, idx_q))
+                ref.self_attention_bwd_dq_rows(qr, dor, rows, kh, vh, w.grid)
         n += rows_per_head
     dt = time.perf_counter() - t0
-    return n, dt
+    per_row = 4.0 * Lk * d * (3.5 if w.kind == "self_fwd_bwd" else 1.0)
+    return n, dt, per_row
 
 
 def cpu_baseline(w, rows_per_head: int):
-    n, dt = _oracle_rows(w, rows_per_head, heads=2)
-    fl = 4.0 * w.L * w.d * n
-    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{n} query rows (2 heads x {rows_per_head}) of {w.name} against all {w.L} keys, "
+    n, dt, per_row = _oracle_rows(w, rows_per_head, heads=2)
+    what = {"self_fwd": "forward", "cross_fwd": "cross-attention forward",
+            "self_fwd_bwd": "forward + dQ backward"}[w.kind]
+    return {"value": round(per_row * n / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} query rows (2 heads x {rows_per_head}) of {w.name}, oracle {what} against all keys, "
                       f"fp64 numpy, {dt:.1f} s", "rows_per_s": round(n / dt, 1)}
 
 
@@ -462,15 +582,15 @@ def run_reference(args, rank, world):
     rows = args.ref_rows
     for _ in range(args.warmup):
         _oracle_rows(w, rows, heads=1)
-    times, n_tot = [], 0
+    times, n_tot, per_row = [], 0, 0.0
     for _ in range(args.steps):
-        n, dt = _oracle_rows(w, rows, heads=1)
+        n, dt, per_row = _oracle_rows(w, rows, heads=1)
         times.append(dt)
         n_tot += n
     dt = sum(times)
-    fl = 4.0 * w.L * w.d * n_tot
+    fl = per_row * n_tot
     value = fl / dt / 1e12
-    sample = f"{rows} query rows of one head per step against all {w.L} keys (fp64 numpy oracle)"
+    sample = f"{rows} query rows of one head per step against all keys (fp64 numpy oracle)"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),

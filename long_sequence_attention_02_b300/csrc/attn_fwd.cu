@@ -137,6 +137,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ int epi_ok[kQTiles][4];  // per-warp epilogue go/stop flags
+  // The first key lengths, read once per CTA instead of at every item.
+  constexpr int kLensCached = 64;
+  __shared__ int lens_sh[kLensCached];
+  if (a.kv_lens != nullptr && threadIdx.x < kLensCached && static_cast<int>(threadIdx.x) < a.B)
+    lens_sh[threadIdx.x] = a.kv_lens[threadIdx.x];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -158,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     x.q0 = qp * (kBlockM * kQTiles);
     x.n_valid = a.Lk;
     if (a.kv_lens != nullptr) {
-      const int v = a.kv_lens[x.b];
+      const int v = x.b < kLensCached ? lens_sh[x.b] : a.kv_lens[x.b];
       x.n_valid = v < 0 ? 0 : (v > a.Lk ? a.Lk : v);
     }
     x.n_tiles = (x.n_valid + kBlockN - 1) / kBlockN;

@@ -51,4 +51,7 @@ WORKLOADS = {
     "wan14b_720p_cross_fwd": Workload("wan14b_720p_cross_fwd", "cross_fwd", 2, latent_grid(81, 720, 1280), 40, Lk=512),
     "wan14b_720p_self_fwd": Workload("wan14b_720p_self_fwd", "self_fwd", 1, latent_grid(81, 720, 1280), 40),
     "train_64x64x64_fwd_bwd": Workload("train_64x64x64_fwd_bwd", "self_fwd_bwd", 1, (64, 64, 64), 12),
+    # Same step at 1/64 of the size (32,768 tokens): small enough for a full
+    # profiler capture of the backward kernel.
+    "train_32x32x32_fwd_bwd": Workload("train_32x32x32_fwd_bwd", "self_fwd_bwd", 1, (32, 32, 32), 12),
 }
