@@ -29,10 +29,10 @@
 //      backward (one 64 KB tile per query tile per CTA); it is done by a
 //      warpgroup of its own so that it overlaps the next tile's softmax.
 // Warps (register budgets moved with setmaxnreg):
-//   0-7    compute (warp w: TMEM lanes 32*(w%4).., column half w/4)   160 regs
+//   0-7    compute (warp w: TMEM lanes 32*(w%4).., column half w/4)   152 regs
 //   8      TMA producer; 9 MMA issuer (warp-converged, one elected lane
 //          issues) and TMEM owner; 10-11 idle                           112 regs
-//   12-15  dQ writers (warp w: TMEM lanes 32*(w%4)..)                    80 regs
+//   12-15  dQ writers (warp w: TMEM lanes 32*(w%4)..)                    96 regs
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -41,9 +41,9 @@ namespace wan {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr uint32_t kComputeRegs = 160;  // 2 x 128 x 160 + 128 x 112 + 128 x 80 = 512 x 128
+constexpr uint32_t kComputeRegs = 152;  // 2 x 128 x 152 + 128 x 112 + 128 x 96 = 512 x 128
 constexpr uint32_t kControlRegs = 112;
-constexpr uint32_t kDqRegs = 80;
+constexpr uint32_t kDqRegs = 96;
 constexpr int kDqWarp0 = 12;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -59,7 +59,7 @@ constexpr int kOffDS = kOffStage + 2 * kStageBytes;
 constexpr int kOffRows = kOffDS + kTileBytes;  // 2 stages of {LSE*log2e[128], D[128]}
 constexpr int kRowsBytes = 2 * kTile * 4;
 constexpr int kOffBar = kOffRows + 2 * kRowsBytes;
-constexpr int kSmemBytes = kOffBar + 256;  // barriers [0,112), TMEM base, abort word, dQ stop flags at 128
+constexpr int kSmemBytes = kOffBar + 256;  // barriers, TMEM base, abort word; dQ stop flags at 192
 
 enum Bar {
   kBarKV = 0,
@@ -69,14 +69,16 @@ enum Bar {
   kBarDP = 6,
   kBarP = 7,
   kBarDS = 8,
-  kBarDQ = 9,
-  kBarDQFree = 10,
+  kBarDQ0 = 9,       // dQ half 0 (d 0..63) is in TMEM (S columns 64..127)
+  kBarDQFree0 = 10,  // ... and has been read: S of the next tile may be written
   kBarAcc = 11,
   kBarDrain = 12,
   kBarDSFree = 13,  // the dS buffer, used as dQ staging after the dQ MMA, is free again
-  kNumBars = 14
+  kBarDQ1 = 14,      // dQ half 1 (d 64..127) is in TMEM (dP columns 64..127)
+  kBarDQFree1 = 15,  // ... and has been read: dP of the next tile may be written
+  kNumBars = 16
 };
-static_assert(kNumBars * 8 + 8 <= 128, "barrier area overlaps the dQ stop flags");
+static_assert(kNumBars * 8 + 8 <= 192, "barrier area overlaps the dQ stop flags");
 
 struct BwdArgs {
   const float* lse2;  // [B*H][Lpad] LSE * log2(e), pad +inf
@@ -149,8 +151,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kBarDP], 1);
     mbar_init(&bars[kBarP], 8);
     mbar_init(&bars[kBarDS], 8);
-    mbar_init(&bars[kBarDQ], 1);
-    mbar_init(&bars[kBarDQFree], 4);
+    mbar_init(&bars[kBarDQ0], 1);
+    mbar_init(&bars[kBarDQ1], 1);
+    mbar_init(&bars[kBarDQFree0], 4);
+    mbar_init(&bars[kBarDQFree1], 4);
     mbar_init(&bars[kBarAcc], 1);
     mbar_init(&bars[kBarDrain], 1);
     mbar_init(&bars[kBarDSFree], 1);
@@ -228,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t so = static_cast<uint64_t>((s * kStageBytes) >> 4);   // Q tile of stage s
         const uint64_t sdo = so + static_cast<uint64_t>(kTileBytes >> 4);      // dO tile of stage s
         ok = warp_wait(&bars[kBarQFull0 + s], use & 1, abort, a.lc.err, to);
-        if (ok && i > 0) ok = warp_wait(&bars[kBarDQFree], (i - 1) & 1, abort, a.lc.err, to);
+        if (ok && i > 0) ok = warp_wait(&bars[kBarDQFree0], (i - 1) & 1, abort, a.lc.err, to);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -237,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ss_elect(tS, dK + off, dStage_k + so + off, id_kk, kk > 0);
         }
         umma_commit_elect(&bars[kBarS]);
+        if (i > 0 && !(ok = warp_wait(&bars[kBarDQFree1], (i - 1) & 1, abort, a.lc.err, to))) break;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
@@ -256,14 +261,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 8; ++kk)
           umma_ts_elect(tDK, tDP + (kk >> 2) * 64 + (kk & 3) * 8, dStage_mn + so + static_cast<uint64_t>(kk * 128),
                         id_tm, (i > 0 || kk > 0) ? 1u : 0u);
-        // dQ_i = dS K_rot, d-halves into S[64,128) and dP[64,128).
+        // dQ_i = dS K_rot, d-halves into S[64,128) and dP[64,128), each with
+        // its own commit so that the dQ warps can start on half 0 early.
 #pragma unroll
-        for (int half = 0; half < 2; ++half)
+        for (int half = 0; half < 2; ++half) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma_ss_elect((half ? tDP : tS) + 64, dDS + static_cast<uint64_t>(kk * 128),
                           dKmn + static_cast<uint64_t>((half * kHalfBytes + kk * 2048) >> 4), id_dq, kk > 0);
-        umma_commit_elect(&bars[kBarDQ]);
+          umma_commit_elect(&bars[half ? kBarDQ1 : kBarDQ0]);
+        }
         umma_commit_elect(&bars[kBarQEmpty0 + s]);
       }
       if (ok) umma_commit_elect(&bars[kBarAcc]);
@@ -279,37 +286,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
     // Per-warp stop flags (in the dynamic barrier area: a static __shared__
     // array would move the 1024-byte aligned dynamic base).
-    volatile int* dq_fail = reinterpret_cast<volatile int*>(smem + kOffBar + 128);
+    volatile int* dq_fail = reinterpret_cast<volatile int*>(smem + kOffBar + 192);
     for (int i = 0; i < nq; ++i) {
-      const bool ok = warp_wait(&bars[kBarDQ], i & 1, abort, a.lc.err, to);
+      const bool ok = warp_wait(&bars[kBarDQ0], i & 1, abort, a.lc.err, to);
       // The four warps decide together whether to stop, so that none of
       // them is left waiting at the named barriers below.
       if (lane == 0) dq_fail[wq] = ok ? 0 : 1;
       named_bar_sync(1, 128);
       if (dq_fail[0] | dq_fail[1] | dq_fail[2] | dq_fail[3]) break;
       tc_fence_after();
-      // dQ leaves TMEM in two halves of 64 columns. Each half is staged in the
-      // dS buffer (free once the dQ MMAs have completed) as two 128-row x
-      // 32-float boxes in the 128-byte swizzled layout, then one elected
-      // thread adds the boxes to the fp32 accumulator with bulk tensor
-      // reductions and waits until they have read the staging buffer.
+      // Both halves leave TMEM before any staging round trip, so the next
+      // tile's S and dP MMAs are held up only by two TMEM loads each. The
+      // staging area is the dS buffer, free once both dQ halves' MMAs (which
+      // read dS) have completed. Each half is staged as two 128-row x
+      // 32-float boxes in the 128-byte swizzled layout and added to the fp32
+      // accumulator by one elected thread with bulk tensor reductions.
       const int qt = i + q_start < nq ? i + q_start : i + q_start - nq;
       uint8_t* stage = smem + kOffDS;
+      uint32_t v[64];
+      tmem_ld32(tS + lane_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(tS + lane_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarDQFree0]);
+      // dQ half 1 is committed right after half 0 with no wait in between;
+      // this wait ignores the abort flag so that all four warps reach the
+      // barriers below (a timeout still raises the error).
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarDQ1], i & 1, nullptr, to)) && lane == 0)
+        raise_abort(abort, a.lc.err);
+      tc_fence_after();
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
-        uint32_t v[64];
-        tmem_ld32((half ? tDP : tS) + lane_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tmem_ld32((half ? tDP : tS) + lane_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-        tmem_ld_wait();
-        if (half == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kBarDQFree]);
-        }
 #pragma unroll
         for (int c = 0; c < 16; ++c)  // box c/8, 16-byte chunk c%8 of row r
           *reinterpret_cast<uint4*>(stage + (c >> 3) * (kTile * 128) + sw128_offset(r, c & 7)) =
               make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        if (half == 0) {
+          tmem_ld32(tDP + lane_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(tDP + lane_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kBarDQFree1]);
+        }
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (warp == kDqWarp0 && lane == 0) {
@@ -349,7 +369,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 2; ++c) {
           load32(tS + lane_addr + ch * 64 + c * 32, sv);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) p[c * 32 + k] = key_ok ? ex2_approx(fmaf(sv[k], sl2, -lse2[c * 32 + k])) : 0.f;
+          for (int k4 = 0; k4 < 8; ++k4) {  // the row values are the same for every lane: 16-byte broadcasts
+            const float4 l4 = reinterpret_cast<const float4*>(lse2)[c * 8 + k4];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int k = 4 * k4 + e;
+              p[c * 32 + k] = key_ok ? ex2_approx(fmaf(sv[k], sl2, -lv[e])) : 0.f;
+            }
+          }
         }
       }
       {
@@ -372,11 +400,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 2; ++c) {
           load32(tDP + lane_addr + ch * 64 + c * 32, dv);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int j0 = c * 32 + 2 * k;
-            const float d0 = p[j0] * (dv[2 * k] - drow[j0]) * a.scale;
-            const float d1 = p[j0 + 1] * (dv[2 * k + 1] - drow[j0 + 1]) * a.scale;
-            pk[c * 16 + k] = pack_bf16x2(d0, d1);
+          for (int k4 = 0; k4 < 8; ++k4) {
+            const float4 d4 = reinterpret_cast<const float4*>(drow)[c * 8 + k4];
+            const int j0 = c * 32 + 4 * k4;
+            pk[c * 16 + 2 * k4] = pack_bf16x2(p[j0] * (dv[4 * k4] - d4.x) * a.scale,
+                                              p[j0 + 1] * (dv[4 * k4 + 1] - d4.y) * a.scale);
+            pk[c * 16 + 2 * k4 + 1] = pack_bf16x2(p[j0 + 2] * (dv[4 * k4 + 2] - d4.z) * a.scale,
+                                                  p[j0 + 3] * (dv[4 * k4 + 3] - d4.w) * a.scale);
           }
         }
         tmem_st32(tDP + lane_addr + ch * 64, pk);
