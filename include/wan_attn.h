@@ -136,6 +136,52 @@ int wan_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
                  float scale, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * One step of Ring attention on one GPU: attention of a chunk of queries over
+ * a chunk of keys of the same video, merged into a running result (anthology
+ * note, Key takeaways, and ctol.digital article, "Speed, Scale, and
+ * Efficiency": Wan trains long sequences with 2D context parallelism, Ring
+ * Attention across devices and Ulysses inside; a Ring step attends to the
+ * K/V chunk it holds and merges the partial result by log-sum-exp).
+ *   q        : [B, q_len, H, 128] bf16, grid tokens q_start .. q_start+q_len-1 (pre-RoPE)
+ *   k, v     : [B, kv_len, H, 128] bf16, grid tokens kv_start .. kv_start+kv_len-1 (k pre-RoPE)
+ *   o, lse   : [B, q_len, H, 128] bf16 and [B, H, q_len] fp32 (lse required)
+ *   accumulate = 0: o, lse <- attention over this K/V chunk.
+ *   accumulate = 1: (o, lse) <- merge of the running (o, lse) with this
+ *              chunk's (O_c, LSE_c): LSE = log(e^lse + e^LSE_c),
+ *              O = (e^lse o + e^LSE_c O_c) / e^LSE. A running lse of -inf
+ *              counts as empty.
+ *   tables   : RoPE tables of grid g (positions are the tokens' grid coordinates)
+ *   workspace: at least wan_attn_workspace_size(WAN_OP_FWD, B, g, H, 128)
+ *              bytes (it holds the chunk's rotated keys).
+ * 0 <= q_start, 1 <= q_len, q_start + q_len <= F*Hp*Wp, and the same for kv.
+ * Stepping over all K/V chunks of a sequence reproduces wan_attn_fwd up to
+ * rounding (o is rounded to bf16 after every step).
+ */
+int wan_attn_fwd_ring_step(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g,
+                           int H, int head_dim, const float* tables, float scale, int q_start, int q_len,
+                           int kv_start, int kv_len, int accumulate, void* workspace, size_t ws_bytes,
+                           void* stream);
+
+/*
+ * Decoupled cross-attention of image-to-video models: the video queries
+ * attend separately to the text tokens and to the image tokens (a CLIP image
+ * embedding projected to the model width) and the two results are added
+ * (anthology note, Key takeaways: the CLIP image embedding enters through
+ * decoupled cross-attention; gojay.top reading, section 6 Extended
+ * Applications and code map ④ WanModel T2V / I2V: two attention paths, then
+ * summed). The pages do not give the number of image tokens.
+ *   q                : [B, Lq, H, 128] bf16, Lq = F*Hp*Wp
+ *   k_txt, v_txt     : [B, Lk_txt, H, 128], lens_txt: device int32 [B] or NULL (all valid)
+ *   k_img, v_img     : [B, Lk_img, H, 128], lens_img: device int32 [B] or NULL
+ *   o                : softmax(q k_txt^T) v_txt + softmax(q k_img^T) v_img (bf16)
+ *   lse              : optional [B, H, Lq], the log-sum-exp of the text path
+ * 1 <= Lk_txt, Lk_img <= 512. No RoPE. Two launches on `stream`.
+ */
+int wan_xattn_fwd_dual(const void* q, const void* k_txt, const void* v_txt, const int32_t* lens_txt, int Lk_txt,
+                       const void* k_img, const void* v_img, const int32_t* lens_img, int Lk_img, void* o,
+                       float* lse, int B, wan_grid_t g, int H, int head_dim, float scale, void* stream);
+
+/*
  * Synchronise `stream`, then return and clear the device error word of the
  * current device: WAN_OK, or WAN_ERR_TIMEOUT if a kernel gave up a bounded
  * wait since the last call (its outputs are then undefined), or WAN_ERR_CUDA

@@ -33,6 +33,7 @@ EXPORTED = (
     "wan_status_str", "wan_version", "wan_rope3d_tables_size", "wan_rope3d_tables",
     "wan_attn_workspace_size", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
     "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall", "wan_attn_fwd_noalloc",
+    "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual",
 )
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 NOALLOC_MAX_ROW_HEADS = NOALLOC_SCRATCH_BYTES // 256
@@ -71,12 +72,16 @@ def load_library(path: str = LIB_PATH):
     lib.wan_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, wan_grid_t, i32, i32, vp, f32, vp, sz,
                                  vp]
     lib.wan_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, wan_grid_t, i32, i32, vp, f32, vp]
+    lib.wan_attn_fwd_ring_step.argtypes = [vp, vp, vp, vp, vp, i32, wan_grid_t, i32, i32, vp, f32, i32, i32, i32,
+                                           i32, i32, vp, sz, vp]
+    lib.wan_xattn_fwd_dual.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, vp, i32, wan_grid_t, i32, i32,
+                                       f32, vp]
     lib.wan_get_device_status.argtypes = [vp]
     lib.wan_debug_inject_stall.argtypes = [i32, i32]
     lib.wan_profile_set_events.argtypes = [vp, vp]
     for name in ("wan_rope3d_tables", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
                  "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall",
-                 "wan_attn_fwd_noalloc"):
+                 "wan_attn_fwd_noalloc", "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -160,6 +165,21 @@ def wan_attn_fwd_noalloc(q, k, v, o, lse, B, grid, H, head_dim, tables, scale, s
     holds the rotated keys (B * L * H <= NOALLOC_MAX_ROW_HEADS)."""
     return load_library().wan_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, _grid(grid), H,
                                                 head_dim, _ptr(tables), float(scale), _stream(stream))
+
+
+def wan_attn_fwd_ring_step(q, k, v, o, lse, B, grid, H, head_dim, tables, scale, q_start, q_len, kv_start, kv_len,
+                           accumulate, workspace, ws_bytes, stream=None) -> int:
+    return load_library().wan_attn_fwd_ring_step(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, _grid(grid), H,
+                                                  head_dim, _ptr(tables), float(scale), int(q_start), int(q_len),
+                                                  int(kv_start), int(kv_len), int(accumulate), _ptr(workspace),
+                                                  int(ws_bytes), _stream(stream))
+
+
+def wan_xattn_fwd_dual(q, k_txt, v_txt, lens_txt, Lk_txt, k_img, v_img, lens_img, Lk_img, o, lse, B, grid, H,
+                       head_dim, scale, stream=None) -> int:
+    return load_library().wan_xattn_fwd_dual(_ptr(q), _ptr(k_txt), _ptr(v_txt), _ptr(lens_txt), int(Lk_txt),
+                                              _ptr(k_img), _ptr(v_img), _ptr(lens_img), int(Lk_img), _ptr(o),
+                                              _ptr(lse), B, _grid(grid), H, head_dim, float(scale), _stream(stream))
 
 
 def wan_get_device_status(stream=None) -> int:

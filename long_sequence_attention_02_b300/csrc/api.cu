@@ -246,6 +246,59 @@ int wan_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
                               workspace, launch_common(*st), static_cast<cudaStream_t>(stream));
 }
 
+int wan_attn_fwd_ring_step(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g,
+                           int H, int head_dim, const float* tables, float scale, int q_start, int q_len,
+                           int kv_start, int kv_len, int accumulate, void* workspace, size_t ws_bytes,
+                           void* stream) {
+  long long L = 0;
+  int rc = grid_tokens(g, &L);
+  if (rc == WAN_OK) rc = check_shapes(B, L, H, head_dim);
+  if (rc != WAN_OK) return rc;
+  if (q_start < 0 || q_len < 1 || (long long)q_start + q_len > L || kv_start < 0 || kv_len < 1 ||
+      (long long)kv_start + kv_len > L || (accumulate != 0 && accumulate != 1))
+    return WAN_ERR_INVALID;
+  if (!q || !k || !v || !o || !lse || !tables || !workspace) return B == 0 ? WAN_OK : WAN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(tables) & 7u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return WAN_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return WAN_ERR_INVALID;
+  if (ws_bytes < round_up((size_t)B * kv_len * H * kHeadDim * 2, 256)) return WAN_ERR_INVALID;
+  if (B == 0) return WAN_OK;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != WAN_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const wan::RopeTables tab = split_tables(tables, g);
+  if (wan::launch_rope_rotate_bf16_rows(k, workspace, B, kv_len, kv_start, g, H, tab, false, s) != cudaSuccess)
+    return WAN_ERR_CUDA;
+  return wan::launch_attn_fwd(q, workspace, v, o, lse, B, q_len, kv_len, H, g, tab, true, nullptr, scale,
+                              launch_common(*st), s, q_start, accumulate ? wan::kMergeLse : wan::kMergeNone);
+}
+
+int wan_xattn_fwd_dual(const void* q, const void* k_txt, const void* v_txt, const int32_t* lens_txt, int Lk_txt,
+                       const void* k_img, const void* v_img, const int32_t* lens_img, int Lk_img, void* o,
+                       float* lse, int B, wan_grid_t g, int H, int head_dim, float scale, void* stream) {
+  long long L = 0;
+  int rc = grid_tokens(g, &L);
+  if (rc == WAN_OK) rc = check_shapes(B, L, H, head_dim);
+  if (rc != WAN_OK) return rc;
+  if (Lk_txt < 1 || Lk_txt > 512 || Lk_img < 1 || Lk_img > 512) return WAN_ERR_INVALID;
+  if (!q || !k_txt || !v_txt || !k_img || !v_img || !o) return B == 0 ? WAN_OK : WAN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_txt) || !aligned16(v_txt) || !aligned16(k_img) || !aligned16(v_img) ||
+      !aligned16(o) || (reinterpret_cast<uintptr_t>(lens_txt) & 3u) || (reinterpret_cast<uintptr_t>(lens_img) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return WAN_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return WAN_ERR_INVALID;
+  if (B == 0) return WAN_OK;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != WAN_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = wan::launch_attn_fwd(q, k_txt, v_txt, o, lse, B, (int)L, Lk_txt, H, g, wan::RopeTables{}, false, lens_txt,
+                            scale, launch_common(*st), s);
+  if (rc != WAN_OK) return rc;
+  return wan::launch_attn_fwd(q, k_img, v_img, o, nullptr, B, (int)L, Lk_img, H, g, wan::RopeTables{}, false,
+                              lens_img, scale, launch_common(*st), s, 0, wan::kMergeAdd);
+}
+
 int wan_get_device_status(void* stream) {
   DeviceState* st = nullptr;
   int rc = device_state(&st);

@@ -72,6 +72,7 @@ struct FwdArgs {
   RopeTables tab;
   int Lq, Lk, H, Hp, Wp, B;
   int n_qpairs;  // 256-row query blocks per (b, h)
+  int q_pos0;    // grid token of query row 0 (a chunk of a longer sequence)
   float scale_log2;
   LaunchCommon lc;
 };
@@ -93,8 +94,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 // Rotate row r of a swizzled [128 x 128] bf16 tile in place by the 3D RoPE
 // angles of token `row`.
 __device__ __forceinline__ void rope_row_in_smem(uint8_t* tile, int r, int row, const FwdArgs& a) {
-  const int w = row % a.Wp;
-  const int tmp = row / a.Wp;
+  const int tok = row + a.q_pos0;
+  const int w = tok % a.Wp;
+  const int tmp = tok / a.Wp;
   const int hh = tmp % a.Hp;
   const int t = tmp / a.Hp;
   const float2* ct = a.tab.t + t * kPairsT;
@@ -118,7 +120,7 @@ __device__ __forceinline__ void rope_row_in_smem(uint8_t* tile, int r, int row, 
   }
 }
 
-template <bool kRope>
+template <bool kRope, int kMerge>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -134,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t bar_kv_full[kStages], bar_kv_empty[kStages];
   __shared__ __align__(8) uint64_t bar_s_full[kQTiles], bar_p_full[kQTiles], bar_o_full[kQTiles];
   __shared__ __align__(8) uint64_t bar_drain;
+  __shared__ __align__(8) uint64_t bar_oldo[kQTiles];  // previous O tile loaded (merging epilogues)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ int epi_ok[kQTiles][4];  // per-warp epilogue go/stop flags
@@ -184,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_s_full[t], 1);
       mbar_init(&bar_p_full[t], 4);
       mbar_init(&bar_o_full[t], 1);
+      mbar_init(&bar_oldo[t], 1);
     }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_kv_full[s], 1);
@@ -360,10 +364,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_addr + t * 128;
     const uint32_t tO = tmem + lane_addr + 256 + t * 128;
     const float sl2 = a.scale_log2;
+    // After a failed wait (ok = false) the warp skips all work but keeps
+    // walking the items, so that the four warps of a tile always execute
+    // the same sequence of named barriers.
     bool ok = true;
     int nq = 0;  // items with key tiles so far
     int sp = 0;  // S/P phases so far
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
       // Only the key-tile counts stay live through the softmax loop; the
       // output addresses are recomputed for the epilogue.
       int n_valid, n_tiles, kv_start;
@@ -373,7 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         n_tiles = x.n_tiles;
         kv_start = x.kv_start;
       }
-      if (n_tiles == 0) {  // no valid key: O = 0, LSE = -inf
+      if (n_tiles == 0) {  // no valid key: O = 0, LSE = -inf (a merge leaves o / lse as they are)
+        if (kMerge != kMergeNone) continue;
         const Item x = item_of(it);
         const int row = x.q0 + t * kBlockM + r;
         if (row < a.Lq) {
@@ -385,10 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int qb = nq % kQBuf;
       if (kRope) {
-        ok = warp_wait(&bar_q_full[qb], (nq / kQBuf) & 1, abort, a.lc.err, to);
-        if (!ok) break;
+        if (ok) ok = warp_wait(&bar_q_full[qb], (nq / kQBuf) & 1, abort, a.lc.err, to);
         const int row = item_of(it).q0 + t * kBlockM + r;
-        if (row < a.Lq) rope_row_in_smem(sQ + (qb * kQTiles + t) * kTileBytes, r, row, a);
+        if (ok && row < a.Lq) rope_row_in_smem(sQ + (qb * kQTiles + t) * kTileBytes, r, row, a);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_q_ready[qb]);
@@ -478,7 +485,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_p_full[t]);
       }
-      if (!ok) break;
 
       // ---------------------------------------------------------- epilogue
       // O_t is normalised into bf16 and staged in this tile's Q buffer (no
@@ -486,41 +492,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       // one thread writes it with two TMA tensor stores and, once they have
       // read the staging area, hands the buffer back to the Q producer. The
       // four warps of the tile agree on stopping before the named barriers.
-      ok = warp_wait(&bar_o_full[t], nq & 1, abort, a.lc.err, to);
+      if (ok) ok = warp_wait(&bar_o_full[t], nq & 1, abort, a.lc.err, to);
       if (lane == 0) epi_ok[t][wq] = ok ? 1 : 0;
       named_bar_sync(1 + t, 128);
-      if (!(epi_ok[t][0] & epi_ok[t][1] & epi_ok[t][2] & epi_ok[t][3])) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+      const bool all_ok = epi_ok[t][0] & epi_ok[t][1] & epi_ok[t][2] & epi_ok[t][3];
+      ok = ok && all_ok;
       const Item x = item_of(it);
-      const int row = x.q0 + t * kBlockM + r;
       uint8_t* stage = sQ + (qb * kQTiles + t) * kTileBytes;
-      const float inv = 1.0f / l;
-      // O_t is read out of TMEM here; the next item's first PV overwrites it
-      // only after this warp signals that item's first P (program order).
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(tO + c * 32, ov);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {  // 16-byte chunk 4c+q of the row: half c/2, chunk (4c+q)%8
-          uint32_t pk[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(ov[8 * q + 2 * i]) * inv, __uint_as_float(ov[8 * q + 2 * i + 1]) * inv);
-          const int chunk = 4 * c + q;
-          *reinterpret_cast<uint4*>(stage + (chunk >> 3) * kHalfBytes + sw128_offset(r, chunk & 7)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      if (all_ok) {
+        tc_fence_after();
+        const int row = x.q0 + t * kBlockM + r;
+        float inv = 1.0f / l;
+        const float lse_new = (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f;  // natural log
+        // Merging epilogues first bring the previous O tile into the staging
+        // area (same swizzled layout as the store); rows past the end read 0.
+        float w_old = 0.f;
+        float lse_out = lse_new;
+        if (kMerge != kMergeNone) {
+          if (wq == 0 && lane == 0) {
+            mbar_arrive_expect_tx(&bar_oldo[t], kTileBytes);
+            tma_load_4d(stage, &tm_o, &bar_oldo[t], 0, x.h, x.q0 + t * kBlockM, x.b);
+            tma_load_4d(stage + kHalfBytes, &tm_o, &bar_oldo[t], 64, x.h, x.q0 + t * kBlockM, x.b);
+          }
+          if (kMerge == kMergeLse && row < a.Lq) {
+            // O = (e^lse_old O_old + e^lse_new O_new) / (e^lse_old + e^lse_new)
+            const float lse_old = a.lse[(static_cast<size_t>(x.b) * a.H + x.h) * a.Lq + row];
+            const float mx = fmaxf(lse_old, lse_new);
+            const float eo = lse_old == -INFINITY ? 0.f : __expf(lse_old - mx);
+            const float en = __expf(lse_new - mx);
+            lse_out = mx + __logf(eo + en);
+            w_old = eo / (eo + en);
+            inv *= en / (eo + en);
+          } else if (kMerge == kMergeAdd) {
+            w_old = 1.f;
+          }
+          // Every warp of the tile waits for the copy (the TMA write of the
+          // staging area happens-before the reads below).
+          ok = warp_wait(&bar_oldo[t], nq & 1, abort, a.lc.err, to) && ok;
         }
+        // O_t is read out of TMEM here; the next item's first PV overwrites it
+        // only after this warp signals that item's first P (program order).
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tO + c * 32, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {  // 16-byte chunk 4c+q of the row: half c/2, chunk (4c+q)%8
+            const int chunk = 4 * c + q;
+            uint4* dst = reinterpret_cast<uint4*>(stage + (chunk >> 3) * kHalfBytes + sw128_offset(r, chunk & 7));
+            float vals[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) vals[i] = __uint_as_float(ov[8 * q + i]) * inv;
+            if (kMerge != kMergeNone) {
+              const uint4 old = *dst;
+              const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                vals[2 * i] = fmaf(w_old, __uint_as_float(ow[i] << 16), vals[2 * i]);
+                vals[2 * i + 1] = fmaf(w_old, __uint_as_float(ow[i] & 0xFFFF0000u), vals[2 * i + 1]);
+              }
+            }
+            *dst = make_uint4(pack_bf16x2(vals[0], vals[1]), pack_bf16x2(vals[2], vals[3]), pack_bf16x2(vals[4], vals[5]),
+                              pack_bf16x2(vals[6], vals[7]));
+          }
+        }
+        if (a.lse && row < a.Lq && kMerge != kMergeAdd)
+          a.lse[(static_cast<size_t>(x.b) * a.H + x.h) * a.Lq + row] = lse_out;
+        fence_proxy_async_smem();
       }
-      if (a.lse && row < a.Lq)
-        a.lse[(static_cast<size_t>(x.b) * a.H + x.h) * a.Lq + row] = (m_ref * sl2 + __log2f(l)) * 0.69314718055994531f;
-      fence_proxy_async_smem();
       named_bar_sync(1 + t, 128);
-      if (wq == 0 && lane == 0) {
+      if (all_ok && wq == 0 && lane == 0) {
         // Rows past the end of the sequence fall outside the tensor map and
         // are not written.
         tma_store_4d(&tm_o, stage, 0, x.h, x.q0 + t * kBlockM, x.b);
@@ -549,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int launch_attn_fwd(const void* q, const void* k_rot, const void* v, void* o, float* lse, int B, int Lq, int Lk,
                     int H, wan_grid_t g, RopeTables tab, bool rope, const int32_t* kv_lens, float scale,
-                    const LaunchCommon& lc, cudaStream_t s) {
+                    const LaunchCommon& lc, cudaStream_t s, int q_pos0, int merge) {
   CUtensorMap tq, tk, tv, to;
   if (!make_tmap_bld(&tq, q, B, Lq, H, kHeadDim, 128)) return WAN_ERR_CUDA;
   if (!make_tmap_bld(&to, o, B, Lq, H, kHeadDim, 128)) return WAN_ERR_CUDA;
@@ -567,6 +609,7 @@ int launch_attn_fwd(const void* q, const void* k_rot, const void* v, void* o, fl
   a.Hp = g.Hp;
   a.Wp = g.Wp;
   a.n_qpairs = (Lq + kBlockM * kQTiles - 1) / (kBlockM * kQTiles);
+  a.q_pos0 = q_pos0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.lc = lc;
   const long long n_items = static_cast<long long>(a.n_qpairs) * H * B;
@@ -576,7 +619,14 @@ int launch_attn_fwd(const void* q, const void* k_rot, const void* v, void* o, fl
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return WAN_ERR_CUDA;
   const int grid = static_cast<int>(n_items < sms ? n_items : sms);  // persistent: one CTA per SM
-  auto kern = rope ? attn_fwd_kernel<true> : attn_fwd_kernel<false>;
+  // Instantiations: self-attention (plain / Ring-step merge) and cross-
+  // attention (plain / added second path).
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const FwdArgs) = nullptr;
+  if (rope && merge == kMergeNone) kern = attn_fwd_kernel<true, kMergeNone>;
+  if (rope && merge == kMergeLse) kern = attn_fwd_kernel<true, kMergeLse>;
+  if (!rope && merge == kMergeNone) kern = attn_fwd_kernel<false, kMergeNone>;
+  if (!rope && merge == kMergeAdd) kern = attn_fwd_kernel<false, kMergeAdd>;
+  if (kern == nullptr) return WAN_ERR_INVALID;
   const int smem_bytes = rope ? FwdCfg<true>::kSmemBytes : FwdCfg<false>::kSmemBytes;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
     return WAN_ERR_CUDA;

@@ -39,16 +39,28 @@ inline void record_stop(const LaunchCommon& lc, cudaStream_t s) {
 cudaError_t launch_rope_rotate_bf16(const void* x, void* y, int B, wan_grid_t g, int H, RopeTables tab,
                                     bool inverse, cudaStream_t s);
 
+// Same for a chunk of L tokens per batch item starting at grid token pos0.
+cudaError_t launch_rope_rotate_bf16_rows(const void* x, void* y, int B, int L, int pos0, wan_grid_t g, int H,
+                                         RopeTables tab, bool inverse, cudaStream_t s);
+
 // y(bf16) = R(pos)^T x(fp32) for [B, L, H, 128]; used for dQ.
 cudaError_t launch_rope_unrotate_f32(const float* x, void* y, int B, wan_grid_t g, int H, RopeTables tab,
                                      cudaStream_t s);
 
+// How the forward epilogue combines this call's result with what o / lse hold.
+enum FwdMerge : int {
+  kMergeNone = 0,  // o, lse <- this call's attention
+  kMergeLse = 1,   // o, lse <- log-sum-exp merge of (o, lse) with this call's (a ring step)
+  kMergeAdd = 2,   // o <- o + this call's attention; lse untouched (summed attention paths)
+};
+
 // Forward attention. With rope = true (self-attention) q is rotated inside the
-// kernel and k_rot must already be rotated; with rope = false it is plain
-// cross-attention over Lk keys with optional per-batch valid lengths.
+// kernel (query row r is grid token q_pos0 + r) and k_rot must already be
+// rotated; with rope = false it is plain cross-attention over Lk keys with
+// optional per-batch valid lengths.
 int launch_attn_fwd(const void* q, const void* k_rot, const void* v, void* o, float* lse, int B, int Lq, int Lk,
                     int H, wan_grid_t g, RopeTables tab, bool rope, const int32_t* kv_lens, float scale,
-                    const LaunchCommon& lc, cudaStream_t s);
+                    const LaunchCommon& lc, cudaStream_t s, int q_pos0 = 0, int merge = kMergeNone);
 
 // Backward. Workspace layout is defined in attn_bwd.cu.
 size_t attn_bwd_workspace_bytes(int B, int L, int H);

@@ -19,16 +19,18 @@ __device__ __forceinline__ float2 rope_cs(const RopeTables& tab, int pair, int t
   return tab.w[w * kPairsW + (pair - kPairsT - kPairsH)];
 }
 
+// x holds L consecutive tokens per batch item, the first one being token
+// pos0 of the grid (pos0 > 0 for a chunk of a longer sequence).
 template <bool kInverse>
 __global__ void __launch_bounds__(256) rope_rotate_kernel(const uint4* x, uint4* y,
                                                           long long n_chunks, int H, int Hp, int Wp, int L,
-                                                          RopeTables tab) {
+                                                          int pos0, RopeTables tab) {
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_chunks; i += stride) {
     const int c = (int)(i & 15);          // chunk within the 128-wide head
     const long long rowhead = i >> 4;     // (b*L + l)*H + h
     const long long bl = rowhead / H;     // b*L + l
-    const int l = (int)(bl % L);
+    const int l = (int)(bl % L) + pos0;
     const int w = l % Wp;
     const int hh = (l / Wp) % Hp;
     const int t = l / (Wp * Hp);
@@ -89,7 +91,11 @@ cudaError_t launch_rope_unrotate_f32(const float* x, void* y, int B, wan_grid_t 
 
 cudaError_t launch_rope_rotate_bf16(const void* x, void* y, int B, wan_grid_t g, int H, RopeTables tab,
                                     bool inverse, cudaStream_t s) {
-  const int L = g.F * g.Hp * g.Wp;
+  return launch_rope_rotate_bf16_rows(x, y, B, g.F * g.Hp * g.Wp, 0, g, H, tab, inverse, s);
+}
+
+cudaError_t launch_rope_rotate_bf16_rows(const void* x, void* y, int B, int L, int pos0, wan_grid_t g, int H,
+                                         RopeTables tab, bool inverse, cudaStream_t s) {
   const long long n_chunks = (long long)B * L * H * (kHeadDim / 8);
   if (n_chunks == 0) return cudaSuccess;
   int dev = 0, sms = 148;
@@ -99,9 +105,11 @@ cudaError_t launch_rope_rotate_bf16(const void* x, void* y, int B, wan_grid_t g,
   long long cap = (long long)sms * 8;  // 8 resident blocks of 256 threads per SM
   const int blocks = (int)(want < cap ? want : cap);
   if (inverse)
-    rope_rotate_kernel<true><<<blocks, 256, 0, s>>>((const uint4*)x, (uint4*)y, n_chunks, H, g.Hp, g.Wp, L, tab);
+    rope_rotate_kernel<true><<<blocks, 256, 0, s>>>((const uint4*)x, (uint4*)y, n_chunks, H, g.Hp, g.Wp, L, pos0,
+                                                     tab);
   else
-    rope_rotate_kernel<false><<<blocks, 256, 0, s>>>((const uint4*)x, (uint4*)y, n_chunks, H, g.Hp, g.Wp, L, tab);
+    rope_rotate_kernel<false><<<blocks, 256, 0, s>>>((const uint4*)x, (uint4*)y, n_chunks, H, g.Hp, g.Wp, L, pos0,
+                                                      tab);
   return cudaGetLastError();
 }
 

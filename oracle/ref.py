@@ -194,6 +194,39 @@ def cross_attention_fwd(q, k, v, kv_lens, scale=None, block=4096):
     return o, lse
 
 
+def decoupled_cross_attention_fwd(q, k_txt, v_txt, lens_txt, k_img, v_img, lens_img, scale=None):
+    """Image-to-video cross-attention: the text path and the image path are
+    attended separately and their outputs added ("Wan Team, Alibaba (2025)"
+    anthology note, Key takeaways: a CLIP image embedding enters through
+    decoupled cross-attention; gojay.top reading, code map (4) WanModel T2V /
+    I2V: two attention paths, then summed). Returns O [B, Lq, H, d] and the
+    text path's LSE [B, H, Lq].
+    """
+    o_t, lse_t = cross_attention_fwd(q, k_txt, v_txt, lens_txt, scale)
+    o_i, _ = cross_attention_fwd(q, k_img, v_img, lens_img, scale)
+    return o_t + o_i, lse_t
+
+
+def self_attention_fwd_chunk(q_rows, q_start, k_chunk, v_chunk, kv_start, grid, theta=DEFAULT_THETA, scale=None):
+    """Attention of consecutive query tokens over consecutive key tokens of one
+    (b, h), with 3D RoPE at the tokens' own grid positions: the partial result
+    one Ring-attention step produces (anthology note, Key takeaways: Ring
+    Attention across devices in the 2D context parallelism).
+
+    q_rows: [m, d] tokens q_start .. q_start+m-1; k_chunk, v_chunk: [n, d]
+    tokens kv_start .. kv_start+n-1. Returns O [m, d] and LSE [m] over those
+    n keys only.
+    """
+    m, d = q_rows.shape
+    n = k_chunk.shape[0]
+    F, Hp, Wp = grid
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    ang = rope_angles(F, Hp, Wp, d, theta)
+    qr = rope_rotate(q_rows, ang[q_start:q_start + m])
+    kr = rope_rotate(k_chunk, ang[kv_start:kv_start + n])
+    return softmax_attention(qr, kr, v_chunk, scale)
+
+
 # ---------------------------------------------------------------------------
 # Backward (for the rectified-flow training step)
 

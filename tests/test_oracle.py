@@ -341,3 +341,68 @@ def test_flop_convention():
     assert ref.attention_flops(1, 40, 75600, 75600, 128) == pytest.approx(1.1705e14, rel=1e-4)
     assert ref.attention_flops(1, 12, 32760, 32760, 128) == pytest.approx(6.594e12, rel=1e-3)
     assert ref.attention_flops(1, 12, 262144, 262144, 128, backward=True) == pytest.approx(1.0555e15, rel=1e-3)
+
+
+# ---------------------------------------------------------------------------
+# Decoupled image/text cross-attention and Ring-attention chunks
+
+
+def test_decoupled_cross_attention_identical_paths_double():
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((2, 9, 2, 16))
+    k = rng.standard_normal((2, 5, 2, 16))
+    v = rng.standard_normal((2, 5, 2, 16))
+    lens = [5, 3]
+    o, lse = ref.decoupled_cross_attention_fwd(q, k, v, lens, k, v, lens)
+    o1, lse1 = ref.cross_attention_fwd(q, k, v, lens)
+    np.testing.assert_allclose(o, 2.0 * o1, rtol=0, atol=1e-14)
+    np.testing.assert_array_equal(lse, lse1)
+
+
+def test_decoupled_cross_attention_empty_image_path_is_text_path():
+    rng = np.random.default_rng(22)
+    q = rng.standard_normal((1, 7, 1, 8))
+    kt, vt = rng.standard_normal((1, 4, 1, 8)), rng.standard_normal((1, 4, 1, 8))
+    ki, vi = rng.standard_normal((1, 6, 1, 8)), 1e6 * rng.standard_normal((1, 6, 1, 8))
+    o, _ = ref.decoupled_cross_attention_fwd(q, kt, vt, [4], ki, vi, [0])
+    # brute force of the text path alone
+    for i in range(7):
+        s = np.array([q[0, i, 0] @ kt[0, j, 0] for j in range(4)]) / math.sqrt(8)
+        p = np.exp(s - s.max())
+        p /= p.sum()
+        np.testing.assert_allclose(o[0, i, 0], p @ vt[0, :, 0], rtol=1e-12, atol=1e-12)
+
+
+def test_ring_chunks_of_all_keys_merge_to_full_attention():
+    grid = (2, 3, 4)
+    L = 24
+    rng = np.random.default_rng(23)
+    q, k, v = (rng.standard_normal((1, L, 1, 12)) for _ in range(3))
+    o_full, lse_full = ref.self_attention_fwd(q, k, v, grid)
+    q_start, m = 5, 11
+    bounds = [0, 7, 8, 19, 24]
+    o_run, lse_run = None, None
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        o_c, lse_c = ref.self_attention_fwd_chunk(q[0, q_start:q_start + m, 0], q_start, k[0, a:b, 0], v[0, a:b, 0],
+                                                  a, grid)
+        if o_run is None:
+            o_run, lse_run = o_c, lse_c
+        else:
+            o_run, lse_run = ref.merge_partials(o_run, lse_run, o_c, lse_c)
+    np.testing.assert_allclose(o_run, o_full[0, q_start:q_start + m, 0], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse_run, lse_full[0, 0, q_start:q_start + m], rtol=1e-13, atol=1e-13)
+
+
+def test_ring_chunk_uses_grid_positions():
+    # Shifting both chunks' token offsets by a whole number of frames keeps the
+    # relative (t, h, w) offsets, hence the result (3D RoPE relativity).
+    grid = (4, 2, 3)
+    rng = np.random.default_rng(24)
+    qr, kc, vc = rng.standard_normal((3, 16)), rng.standard_normal((5, 16)), rng.standard_normal((5, 16))
+    o1, l1 = ref.self_attention_fwd_chunk(qr, 0, kc, vc, 6, grid)
+    o2, l2 = ref.self_attention_fwd_chunk(qr, 6, kc, vc, 12, grid)
+    np.testing.assert_allclose(o1, o2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=1e-12, atol=1e-12)
+    # ...but a shift of one token (changing w) does not.
+    o3, _ = ref.self_attention_fwd_chunk(qr, 1, kc, vc, 6, grid)
+    assert np.abs(o3 - o1).max() > 1e-3
