@@ -114,3 +114,68 @@ def test_decoupled_cross_attention(lens_txt, Lk_txt, lens_img, Lk_img):
     o_ref, lse_ref = ref.decoupled_cross_attention_fwd(f64(qb), f64(ktb), f64(vtb), lt, f64(kib), f64(vib), li)
     compare(dev_to_f64(o), o_ref, "O (text + image)")
     compare(dev_to_f64(lse), lse_ref, "LSE (text path)")
+
+
+# ---------------------------------------------------------------------------
+# Full-size cases on 4096 seeded sampled rows
+
+
+def _sample(seed, B, H, L, n=4096):
+    rng = np.random.default_rng(seed)
+    flat = rng.choice(B * H * L, size=min(n, B * H * L), replace=False)
+    return flat // (H * L), (flat // L) % H, flat % L
+
+
+def test_ring_steps_480p_sampled():
+    """The 32,760-token, 12-head grid: the middle third of the queries over
+    three K/V chunks (one of them ragged), against the oracle's full rows."""
+    from long_sequence_attention_02_b300.workloads import WORKLOADS
+
+    w = WORKLOADS["wan1.3b_480p_self_fwd"]
+    B, L, H, grid = w.B, w.L, w.H, w.grid
+    shape = (B, L, H, 128)
+    qb, kb, vb = (bits(5, s, shape) for s in (synth.STREAM_Q, synth.STREAM_K, synth.STREAM_V))
+    q_start, q_len = 10920, 10920
+    o, lse = _ring(qb, kb, vb, grid, q_start, q_len, [0, 12000, 12001, L])
+    bs, hs, is_ = _sample(6, B, H, q_len)
+    o_rows, lse_rows = o[bs, is_, hs], lse[bs, hs, is_]
+    r_o, r_l = np.zeros_like(o_rows), np.zeros_like(lse_rows)
+    for bh in sorted(set(zip(bs.tolist(), hs.tolist()))):
+        sel = np.where((bs == bh[0]) & (hs == bh[1]))[0]
+        tok = q_start + is_[sel]
+        r_o[sel], r_l[sel] = ref.self_attention_fwd_rows(f64(qb[bh[0], tok, bh[1]]), tok, f64(kb[bh[0], :, bh[1]]),
+                                                         f64(vb[bh[0], :, bh[1]]), grid)
+    compare(o_rows, r_o, "ring O (480p)")
+    compare(lse_rows, r_l, "ring LSE (480p)")
+
+
+def test_decoupled_cross_attention_full_size_sampled():
+    """2 x 75,600 video queries, 40 heads; 512 text keys (seeded lengths) and
+    257 image keys."""
+    from long_sequence_attention_02_b300.workloads import WORKLOADS
+
+    w = WORKLOADS["wan14b_720p_cross_fwd"]
+    B, Lq, H, Lt, Li = w.B, w.L, w.H, w.Lk, 257
+    qb = bits(7, synth.STREAM_Q, (B, Lq, H, 128))
+    ktb, vtb = bits(7, synth.STREAM_K, (B, Lt, H, 128)), bits(7, synth.STREAM_V, (B, Lt, H, 128))
+    kib, vib = bits(8, synth.STREAM_K, (B, Li, H, 128)), bits(8, synth.STREAM_V, (B, Li, H, 128))
+    lens = synth.kv_lens(7, B)
+    q = to_dev(qb)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, Lq, dtype=torch.float32, device="cuda")
+    wan.check(wan.wan_xattn_fwd_dual(q, to_dev(ktb), to_dev(vtb), torch.from_numpy(lens).cuda(), Lt, to_dev(kib),
+                                     to_dev(vib), None, Li, o, lse, B, w.grid, H, 128, 1 / math.sqrt(128)), "dual")
+    wan.check(wan.wan_get_device_status())
+    bs, hs, is_ = _sample(9, B, H, Lq)
+    o_rows, lse_rows = dev_to_f64(o[bs, is_, hs]), dev_to_f64(lse[bs, hs, is_])
+    r_o, r_l = np.zeros_like(o_rows), np.zeros_like(lse_rows)
+    sc = 1 / math.sqrt(128)
+    for bh in sorted(set(zip(bs.tolist(), hs.tolist()))):
+        b, h = bh
+        sel = np.where((bs == b) & (hs == h))[0]
+        qr = f64(qb[b, is_[sel], h])
+        o1, l1 = ref.softmax_attention(qr, f64(ktb[b, :, h]), f64(vtb[b, :, h]), sc, lens[b])
+        o2, _ = ref.softmax_attention(qr, f64(kib[b, :, h]), f64(vib[b, :, h]), sc, Li)
+        r_o[sel], r_l[sel] = o1 + o2, l1
+    compare(o_rows, r_o, "dual O (full size)")
+    compare(lse_rows, r_l, "dual LSE (full size)")
