@@ -218,6 +218,19 @@ def make_case(wan, torch, dev, w, rank, peaks):
             c.flops, c.kernel, c.kernel_flops, c.launches = fwd_flops, "attn_fwd_kernel<true>", fwd_flops, 2
             c.hbm_bytes = None
             c.bound = "tensor"
+        elif w.kind == "self_fwd_fp8":
+            ws8 = wan.wan_attn_workspace_size(wan.WAN_OP_FWD_FP8, B, grid, H, d)
+            ws = torch.empty(ws8, dtype=torch.uint8, device=dev)
+
+            def run():
+                wan.check(wan.wan_attn_fwd_fp8(q, k, v, o, lse, B, grid, H, d, tables, scale, ws, ws8, stream))
+
+            c.inputs, c.outputs = [q, k, v], [o, lse]
+            # amax pass, quantisation pass, attention
+            c.flops, c.kernel, c.kernel_flops, c.launches = fwd_flops, "attn_fwd_fp8_kernel", fwd_flops, 3
+            c.hbm_bytes = None
+            c.bound = "tensor_fp8"
+            c.dtype = "e4m3"
         else:  # forward + backward (one training step of the attention)
             do = torch.randn(B, L, H, d, device=dev, generator=gen).bfloat16()
             dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
@@ -340,7 +353,16 @@ def run_ours(args, rank, world, local):
         also = extras(wan, torch, dev, peaks, skip=w.name)
 
     traffic = read_traffic(c.kernel, w.name)
-    if c.bound == "tensor":
+    if c.bound == "tensor_fp8":
+        # fp8 dense peak: the measured bf16 GEMM peak x the nominal fp8/bf16 ratio (4.5 / 2.25 PF)
+        peak = 2.0 * peaks["bf16_tflops_sustained"]
+        achieved = c.kernel_flops / (kernel_ms / 1e3) / 1e12
+        roofline = {"bound": "tensor", "kernel": c.kernel, "achieved": round(achieved, 2), "peak": peak,
+                    "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "peak_kind": f"fp8 = 2 x bf16 sustained ({peaks['source']}; nominal 4.5 / 2.25 PF)",
+                    "frac_of_4.5PF_fp8_spec": round(achieved / 4500.0, 4),
+                    "kernel_ms": round(kernel_ms, 3), "traffic": traffic}
+    elif c.bound == "tensor":
         peak = peaks["bf16_tflops_sustained"]
         achieved = c.kernel_flops / (kernel_ms / 1e3) / 1e12
         roofline = {"bound": "tensor", "kernel": c.kernel, "achieved": round(achieved, 2), "peak": peak,
@@ -374,7 +396,7 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": getattr(c, "dtype", "bf16"),
         "data": "synthetic: bf16 N(0,1) inputs (torch generator, seed 1000+rank)",
         "config": config,
         "roofline": roofline,
@@ -515,6 +537,7 @@ KERNEL_SOURCES = {
     "attn_fwd_kernel<true>": ("attn_fwd.cu", "common.cuh"),
     "attn_fwd_kernel<false>": ("attn_fwd.cu", "common.cuh"),
     "attn_bwd_kernel": ("attn_bwd.cu", "common.cuh"),
+    "attn_fwd_fp8_kernel": ("attn_fwd_fp8.cu", "common.cuh"),
 }
 
 
@@ -566,7 +589,7 @@ def _oracle_rows(w, rows_per_head: int, heads: int, seed: int = 0):
 
 def cpu_baseline(w, rows_per_head: int):
     n, dt, per_row = _oracle_rows(w, rows_per_head, heads=2)
-    what = {"self_fwd": "forward", "cross_fwd": "cross-attention forward",
+    what = {"self_fwd": "forward", "self_fwd_fp8": "forward", "cross_fwd": "cross-attention forward",
             "self_fwd_bwd": "forward + dQ backward"}[w.kind]
     return {"value": round(per_row * n / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{n} query rows (2 heads x {rows_per_head}) of {w.name}, oracle {what} against all keys, "

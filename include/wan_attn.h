@@ -56,7 +56,7 @@ enum {
   WAN_ERR_TIMEOUT = 4      /* a device-side bounded wait expired (reported by wan_get_device_status) */
 };
 
-enum { WAN_OP_FWD = 0, WAN_OP_BWD = 1 };
+enum { WAN_OP_FWD = 0, WAN_OP_BWD = 1, WAN_OP_FWD_FP8 = 2 };
 
 /* Latent token grid: F latent frames x Hp x Wp patches, L = F * Hp * Wp. */
 typedef struct {
@@ -87,9 +87,10 @@ size_t wan_rope3d_tables_size(wan_grid_t g, int head_dim);
 int wan_rope3d_tables(wan_grid_t g, int head_dim, double theta, float* tables_dev, void* stream);
 
 /*
- * Workspace bytes for op WAN_OP_FWD (self-attention forward: RoPE'd keys) or
+ * Workspace bytes for op WAN_OP_FWD (self-attention forward: RoPE'd keys),
  * WAN_OP_BWD (backward: rotated Q and K, the fp32 dQ accumulator and the row
- * dot products D = rowsum(dO * O)).
+ * dot products D = rowsum(dO * O)) or WAN_OP_FWD_FP8 (FP8 forward: e4m3 Q, K,
+ * transposed V and the per-head scales).
  */
 size_t wan_attn_workspace_size(int op, int B, wan_grid_t g, int H, int head_dim);
 
@@ -134,6 +135,21 @@ int wan_xattn_fwd(const void* q, const void* k, const void* v, const int32_t* kv
 int wan_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                  void* dq, void* dk, void* dv, int B, wan_grid_t g, int H, int head_dim, const float* tables,
                  float scale, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * FP8 self-attention forward with 3D RoPE (anthology note, Key takeaways:
+ * FP8 attention; ctol.digital article, "Speed, Scale, and Efficiency": FP8
+ * quantisation among the inference speed-ups). Same arguments, layouts and
+ * results as wan_attn_fwd; internally Q_rot, K_rot and V are quantised to
+ * e4m3 with one scale per (b, h) and tensor (amax / 448), P to e4m3, and both
+ * MMAs run as kind::f8f6f4 with fp32 accumulation. Accuracy is that of e4m3
+ * (3 mantissa bits), about 7% relative RMS error on O for N(0,1) inputs.
+ *   workspace: at least wan_attn_workspace_size(WAN_OP_FWD_FP8, B, g, H, 128) bytes
+ * lse is required to be 4-byte aligned when given (it may be NULL).
+ */
+int wan_attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g, int H,
+                     int head_dim, const float* tables, float scale, void* workspace, size_t ws_bytes,
+                     void* stream);
 
 /*
  * One step of Ring attention on one GPU: attention of a chunk of queries over

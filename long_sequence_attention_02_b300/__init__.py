@@ -26,6 +26,7 @@ WAN_ERR_CUDA = 3
 WAN_ERR_TIMEOUT = 4
 WAN_OP_FWD = 0
 WAN_OP_BWD = 1
+WAN_OP_FWD_FP8 = 2
 HEAD_DIM = 128
 DEFAULT_THETA = 10000.0
 
@@ -33,7 +34,7 @@ EXPORTED = (
     "wan_status_str", "wan_version", "wan_rope3d_tables_size", "wan_rope3d_tables",
     "wan_attn_workspace_size", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
     "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall", "wan_attn_fwd_noalloc",
-    "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual",
+    "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual", "wan_attn_fwd_fp8",
 )
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 NOALLOC_MAX_ROW_HEADS = NOALLOC_SCRATCH_BYTES // 256
@@ -72,6 +73,7 @@ def load_library(path: str = LIB_PATH):
     lib.wan_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, wan_grid_t, i32, i32, vp, f32, vp, sz,
                                  vp]
     lib.wan_attn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, wan_grid_t, i32, i32, vp, f32, vp]
+    lib.wan_attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i32, wan_grid_t, i32, i32, vp, f32, vp, sz, vp]
     lib.wan_attn_fwd_ring_step.argtypes = [vp, vp, vp, vp, vp, i32, wan_grid_t, i32, i32, vp, f32, i32, i32, i32,
                                            i32, i32, vp, sz, vp]
     lib.wan_xattn_fwd_dual.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, vp, i32, wan_grid_t, i32, i32,
@@ -81,7 +83,7 @@ def load_library(path: str = LIB_PATH):
     lib.wan_profile_set_events.argtypes = [vp, vp]
     for name in ("wan_rope3d_tables", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
                  "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall",
-                 "wan_attn_fwd_noalloc", "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual"):
+                 "wan_attn_fwd_noalloc", "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual", "wan_attn_fwd_fp8"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -167,6 +169,12 @@ def wan_attn_fwd_noalloc(q, k, v, o, lse, B, grid, H, head_dim, tables, scale, s
                                                 head_dim, _ptr(tables), float(scale), _stream(stream))
 
 
+def wan_attn_fwd_fp8(q, k, v, o, lse, B, grid, H, head_dim, tables, scale, workspace, ws_bytes, stream=None) -> int:
+    return load_library().wan_attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, _grid(grid), H,
+                                            head_dim, _ptr(tables), float(scale), _ptr(workspace), int(ws_bytes),
+                                            _stream(stream))
+
+
 def wan_attn_fwd_ring_step(q, k, v, o, lse, B, grid, H, head_dim, tables, scale, q_start, q_len, kv_start, kv_len,
                            accumulate, workspace, ws_bytes, stream=None) -> int:
     return load_library().wan_attn_fwd_ring_step(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, _grid(grid), H,
@@ -245,6 +253,22 @@ def cross_attention_forward(q, k, v, kv_lens, grid, scale=None, lse=True, stream
     o = torch.empty_like(q)
     lse_t = torch.empty(B, H, Lq, dtype=torch.float32, device=q.device) if lse else None
     check(wan_xattn_fwd(q, k, v, kv_lens, Lk, o, lse_t, B, grid, H, d, scale, stream), "wan_xattn_fwd")
+    return o, lse_t
+
+
+def attention_forward_fp8(q, k, v, grid, tables=None, scale=None, theta=DEFAULT_THETA, lse=True, stream=None):
+    """FP8 (e4m3) self-attention with 3D RoPE. q, k, v: bf16 [B, L, H, 128] on the GPU."""
+    import torch
+
+    B, L, H, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if tables is None:
+        tables = rope_tables(grid, theta, q.device, stream)
+    o = torch.empty_like(q)
+    lse_t = torch.empty(B, H, L, dtype=torch.float32, device=q.device) if lse else None
+    ws_bytes = wan_attn_workspace_size(WAN_OP_FWD_FP8, B, grid, H, d)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    check(wan_attn_fwd_fp8(q, k, v, o, lse_t, B, grid, H, d, tables, scale, ws, ws_bytes, stream), "wan_attn_fwd_fp8")
     return o, lse_t
 
 

@@ -179,6 +179,7 @@ size_t wan_attn_workspace_size(int op, int B, wan_grid_t g, int H, int head_dim)
   if (grid_tokens(g, &L) != WAN_OK || check_shapes(B, L, H, head_dim) != WAN_OK) return 0;
   if (op == WAN_OP_FWD) return round_up((size_t)B * L * H * kHeadDim * 2, 256);
   if (op == WAN_OP_BWD) return wan::attn_bwd_workspace_bytes(B, (int)L, H);
+  if (op == WAN_OP_FWD_FP8) return wan::attn_fwd_fp8_workspace_bytes(B, (int)L, H);
   return 0;
 }
 
@@ -244,6 +245,26 @@ int wan_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
   if ((rc = device_state(&st)) != WAN_OK) return rc;
   return wan::launch_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, g, H, split_tables(tables, g), scale,
                               workspace, launch_common(*st), static_cast<cudaStream_t>(stream));
+}
+
+int wan_attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g, int H,
+                     int head_dim, const float* tables, float scale, void* workspace, size_t ws_bytes,
+                     void* stream) {
+  long long L = 0;
+  int rc = grid_tokens(g, &L);
+  if (rc == WAN_OK) rc = check_shapes(B, L, H, head_dim);
+  if (rc != WAN_OK) return rc;
+  if (!q || !k || !v || !o || !tables || !workspace) return B == 0 ? WAN_OK : WAN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(tables) & 7u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return WAN_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return WAN_ERR_INVALID;
+  if (ws_bytes < wan_attn_workspace_size(WAN_OP_FWD_FP8, B, g, H, head_dim)) return WAN_ERR_INVALID;
+  if (B == 0) return WAN_OK;
+  DeviceState* st = nullptr;
+  if ((rc = device_state(&st)) != WAN_OK) return rc;
+  return wan::launch_attn_fwd_fp8(q, k, v, o, lse, B, g, H, split_tables(tables, g), scale, workspace,
+                                  launch_common(*st), static_cast<cudaStream_t>(stream));
 }
 
 int wan_attn_fwd_ring_step(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g,

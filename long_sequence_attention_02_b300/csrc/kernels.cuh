@@ -62,6 +62,12 @@ int launch_attn_fwd(const void* q, const void* k_rot, const void* v, void* o, fl
                     int H, wan_grid_t g, RopeTables tab, bool rope, const int32_t* kv_lens, float scale,
                     const LaunchCommon& lc, cudaStream_t s, int q_pos0 = 0, int merge = kMergeNone);
 
+// FP8 (e4m3) self-attention forward with per-head scales; the workspace
+// holds Q8, K8, the transposed V8 and the per-head amax (attn_fwd_fp8.cu).
+size_t attn_fwd_fp8_workspace_bytes(int B, int L, int H);
+int launch_attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g, int H,
+                        RopeTables tab, float scale, void* workspace, const LaunchCommon& lc, cudaStream_t s);
+
 // Backward. Workspace layout is defined in attn_bwd.cu.
 size_t attn_bwd_workspace_bytes(int B, int L, int H);
 int launch_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,

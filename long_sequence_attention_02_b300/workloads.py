@@ -25,7 +25,7 @@ def latent_grid(frames: int, height: int, width: int):
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str            # "self_fwd", "cross_fwd" or "self_fwd_bwd"
+    kind: str            # "self_fwd", "self_fwd_fp8", "cross_fwd" or "self_fwd_bwd"
     B: int
     grid: tuple          # (F, Hp, Wp) of the queries
     H: int
@@ -50,6 +50,9 @@ WORKLOADS = {
     "wan1.3b_480p_self_fwd": Workload("wan1.3b_480p_self_fwd", "self_fwd", 1, latent_grid(81, 480, 832), 12),
     "wan14b_720p_cross_fwd": Workload("wan14b_720p_cross_fwd", "cross_fwd", 2, latent_grid(81, 720, 1280), 40, Lk=512),
     "wan14b_720p_self_fwd": Workload("wan14b_720p_self_fwd", "self_fwd", 1, latent_grid(81, 720, 1280), 40),
+    # The same 75,600-token, 40-head forward computed in FP8 (e4m3).
+    "wan14b_720p_self_fwd_fp8": Workload("wan14b_720p_self_fwd_fp8", "self_fwd_fp8", 1, latent_grid(81, 720, 1280),
+                                         40),
     "train_64x64x64_fwd_bwd": Workload("train_64x64x64_fwd_bwd", "self_fwd_bwd", 1, (64, 64, 64), 12),
     # Same step at 1/64 of the size (32,768 tokens): small enough for a full
     # profiler capture of the backward kernel.
