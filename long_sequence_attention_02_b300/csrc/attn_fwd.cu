@@ -33,9 +33,11 @@
 // S_t(j+1) is signalled. The same ordering lets an item's first PV, which
 // overwrites O_t, follow the previous item's epilogue: the softmax warps read
 // O_t out of TMEM before they signal the new item's first P.
-// Softmax keeps a per-row reference max m and rescales O (in TMEM) and l only
-// when the tile max exceeds m by more than 2^8 in the exp2 domain; the final
-// O / l is exact for any reference, and p <= 256 stays well inside bf16.
+// Softmax keeps a per-row reference m: the row maximum of the item's first
+// key tile. Later tiles are exponentiated against m without their own
+// maximum; only a tile whose row sum of p exceeds 256 (its maximum grew by
+// about 2^8) moves m, rescales O (in TMEM) and l, and is recomputed. The
+// final O / l is exact for any reference, and p <= 256 stays well inside bf16.
 #include <climits>
 
 #include "common.cuh"
@@ -63,7 +65,7 @@ struct FwdCfg {
   static constexpr int kStages = kRope ? 4 : 3;
   static constexpr int kSmemBytes = (kQBuf * kQTiles + kStages) * kTileBytes + 1024;
 };
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kTileSumBound = 256.0f;  // see the softmax's reference maximum
 
 struct FwdArgs {
   __nv_bfloat16* o;
@@ -419,65 +421,74 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 128; ++i)
             if (i >= valid) sr[i >> 5][i & 31] = __float_as_uint(-INFINITY);
         }
-        // Row max: four independent chains of three-input maxima.
-        float mc[4];
+        // Reference maximum. The item's first key tile sets m_ref to its row
+        // maximum; later tiles are exponentiated against m_ref without taking
+        // their own maximum. A tile whose row sum of P stays <= kTileSumBound
+        // has every P <= kTileSumBound, so O and l stay well inside fp32; a
+        // row whose sum exceeds it (its maximum grew by about 2^8 or more)
+        // moves m_ref to the tile's maximum, rescales O and l, and the tile
+        // is recomputed. The result is the same softmax for any m_ref.
+        auto row_max = [&]() {
+          float mc[4];  // four independent chains of three-input maxima
 #pragma unroll
-        for (int q = 0; q < 4; ++q) mc[q] = WAN_S(q);
+          for (int q = 0; q < 4; ++q) mc[q] = WAN_S(q);
 #pragma unroll
-        for (int i = 4; i < 128; i += 8) {
+          for (int i = 4; i < 128; i += 8) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            mc[q] = max3f(mc[q], WAN_S(i + 2 * q), WAN_S(i + 2 * q + 1));
-        }
-        const float mx = max3f(mc[0], mc[1], fmaxf(mc[2], mc[3]));
-        const float m_new = fmaxf(m_ref, mx);
-        if (j == 0) {
+            for (int q = 0; q < 4; ++q)
+              mc[q] = max3f(mc[q], WAN_S(i + 2 * q), WAN_S(i + 2 * q + 1));
+          }
+          return max3f(mc[0], mc[1], fmaxf(mc[2], mc[3]));
+        };
+        if (j == 0) m_ref = row_max();
+        float lsum = 0.f;
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+          // p = 2^(s * scale * log2(e) - m * scale * log2(e)), two lanes per f32x2 op.
+          const float neg = -m_ref * sl2;
+          const uint64_t sl2x2 = f2_pack(sl2, sl2);
+          const uint64_t negx2 = f2_pack(neg, neg);
+          uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int e = c * 32 + 2 * i;
+              const uint64_t xx = f2_fma(f2_pack(WAN_S(e), WAN_S(e + 1)), sl2x2, negx2);
+              float x0, x1;
+              f2_unpack(xx, x0, x1);
+              const float p0 = ex2_approx(x0);
+              const float p1 = ex2_approx(x1);
+              const uint64_t pp = f2_pack(p0, p1);
+              acc[i & 1] = f2_add(acc[i & 1], pp);
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16(tS + c * 16, pk);
+          }
+          float a0, a1, a2, a3;
+          f2_unpack(acc[0], a0, a1);
+          f2_unpack(acc[1], a2, a3);
+          lsum = (a0 + a1) + (a2 + a3);
+          const bool need = !(lsum <= kTileSumBound);
+          if (pass == 1 || !__any_sync(0xffffffffu, need)) break;
+          // Rare path: new reference for the rows that need one (alpha = 1
+          // for the others), O and l rescaled, then the tile again.
+          const float m_new = need ? fmaxf(m_ref, row_max()) : m_ref;
+          const float alpha = ex2_approx((m_ref - m_new) * sl2);
+          l *= alpha;
           m_ref = m_new;
-        } else {
-          const bool need = (m_new - m_ref) * sl2 > kRescaleThreshold;
-          if (__any_sync(0xffffffffu, need)) {
-            const float alpha = need ? ex2_approx((m_ref - m_new) * sl2) : 1.0f;
-            if (need) {
-              l *= alpha;
-              m_ref = m_new;
-            }
+          tmem_st_wait();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + c * 32, ov);
+            tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint32_t ov[32];
-              tmem_ld32(tO + c * 32, ov);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-              tmem_st32(tO + c * 32, ov);
-            }
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(tO + c * 32, ov);
           }
         }
-        // p = 2^(s * scale * log2(e) - m * scale * log2(e)), two lanes per f32x2 op.
-        const float neg = -m_ref * sl2;
-        const uint64_t sl2x2 = f2_pack(sl2, sl2);
-        const uint64_t negx2 = f2_pack(neg, neg);
-        uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int e = c * 32 + 2 * i;
-            const uint64_t xx = f2_fma(f2_pack(WAN_S(e), WAN_S(e + 1)), sl2x2, negx2);
-            float x0, x1;
-            f2_unpack(xx, x0, x1);
-            const float p0 = ex2_approx(x0);
-            const float p1 = ex2_approx(x1);
-            const uint64_t pp = f2_pack(p0, p1);
-            acc[i & 1] = f2_add(acc[i & 1], pp);
-            pk[i] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(tS + c * 16, pk);
-        }
-        float a0, a1, a2, a3;
-        f2_unpack(acc[0], a0, a1);
-        f2_unpack(acc[1], a2, a3);
-        const float lsum = (a0 + a1) + (a2 + a3);
 #undef WAN_S
         l += lsum;
         tmem_st_wait();

@@ -7,8 +7,8 @@
 // this file implements the plain per-head reading:
 //   sq = amax|Q_rot| / 448, sk = amax|K_rot| / 448, sv = amax|V| / 448 for each (b, h);
 //   Q8 = e4m3(Q_rot / sq), K8 = e4m3(K_rot / sk), V8 = e4m3(V / sv);
-//   S = sq sk scale (Q8 K8^T);  P = 2^(S log2 e - m log2 e) with the running max m;
-//   P8 = e4m3(P) (P <= 2^8 < 448);  O = sv (P8 V8) / l,  l = sum of the fp32 P;
+//   S = sq sk scale (Q8 K8^T);  P = 2^(S log2 e - m log2 e) with a running reference m;
+//   P8 = e4m3(P) (P <= 256 < 448);  O = sv (P8 V8) / l,  l = sum of the fp32 P;
 // every e4m3 rounding is to nearest even, saturating at +-448.
 //
 // Steps: fp8_amax_kernel (per-head amax of the rotated Q, K and of V),
@@ -40,7 +40,7 @@ constexpr int kLoadWarp8 = 8;
 constexpr int kMmaWarp8 = 9;
 constexpr int kQLoadWarp8 = 10;
 constexpr int kSmemBytes8 = (kQTiles + kStages8) * kTile8Bytes + 1024;
-constexpr float kRescaleThreshold8 = 8.0f;  // log2 units
+constexpr float kTileSumBound = 256.0f;  // see the softmax's reference maximum
 constexpr float kE4m3Max = 448.0f;
 
 struct Fp8Args {
@@ -434,65 +434,73 @@ __global__ void __launch_bounds__(kThreads8, 1)
           for (int i = 0; i < 128; ++i)
             if (i >= valid_last) sr[i >> 5][i & 31] = __float_as_uint(-INFINITY);
         }
-        float mc[4];
+        // Reference maximum as in the bf16 kernel: the item's first key tile
+        // sets m_ref; a later tile whose row sum of P stays <= kTileSumBound
+        // has every P <= kTileSumBound < 448, inside the e4m3 range, and
+        // needs no maximum of its own; a row above the bound moves m_ref to
+        // the tile's maximum, rescales O and l, and the tile is recomputed.
+        auto row_max = [&]() {
+          float mc[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) mc[q] = WAN_S(q);
+          for (int q = 0; q < 4; ++q) mc[q] = WAN_S(q);
 #pragma unroll
-        for (int i = 4; i < 128; i += 8) {
+          for (int i = 4; i < 128; i += 8) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) mc[q] = max3f(mc[q], WAN_S(i + 2 * q), WAN_S(i + 2 * q + 1));
-        }
-        const float m_new = fmaxf(m_ref, max3f(mc[0], mc[1], fmaxf(mc[2], mc[3])));
-        if (j == 0) {
+            for (int q = 0; q < 4; ++q) mc[q] = max3f(mc[q], WAN_S(i + 2 * q), WAN_S(i + 2 * q + 1));
+          }
+          return max3f(mc[0], mc[1], fmaxf(mc[2], mc[3]));
+        };
+        if (j == 0) m_ref = row_max();
+        float tsum = 0.f;
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+          const float neg = -m_ref * sl2;
+          const uint64_t sl2x2 = f2_pack(sl2, sl2);
+          const uint64_t negx2 = f2_pack(neg, neg);
+          uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {  // keys c*32 + 4i .. +3 -> one TMEM column
+              const int e = c * 32 + 4 * i;
+              float p[4];
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const uint64_t xx = f2_fma(f2_pack(WAN_S(e + 2 * u), WAN_S(e + 2 * u + 1)), sl2x2, negx2);
+                float x0, x1;
+                f2_unpack(xx, x0, x1);
+                p[2 * u] = ex2_approx(x0);
+                p[2 * u + 1] = ex2_approx(x1);
+                acc[u] = f2_add(acc[u], f2_pack(p[2 * u], p[2 * u + 1]));
+              }
+              pk[i] = pack_e4m3x4(p[0], p[1], p[2], p[3]);
+            }
+            tmem_st8(tS + c * 8, pk);
+          }
+          float a0, a1, a2, a3;
+          f2_unpack(acc[0], a0, a1);
+          f2_unpack(acc[1], a2, a3);
+          tsum = (a0 + a1) + (a2 + a3);
+          const bool need = !(tsum <= kTileSumBound);
+          if (pass == 1 || !__any_sync(0xffffffffu, need)) break;
+          const float m_new = need ? fmaxf(m_ref, row_max()) : m_ref;
+          const float alpha = ex2_approx((m_ref - m_new) * sl2);  // 1 where no new reference
+          l *= alpha;
           m_ref = m_new;
-        } else {
-          const bool need = (m_new - m_ref) * sl2 > kRescaleThreshold8;
-          if (__any_sync(0xffffffffu, need)) {
-            const float alpha = need ? ex2_approx((m_ref - m_new) * sl2) : 1.0f;
-            if (need) {
-              l *= alpha;
-              m_ref = m_new;
-            }
+          tmem_st_wait();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + c * 32, ov);
+            tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint32_t ov[32];
-              tmem_ld32(tO + c * 32, ov);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-              tmem_st32(tO + c * 32, ov);
-            }
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(tO + c * 32, ov);
           }
         }
-        const float neg = -m_ref * sl2;
-        const uint64_t sl2x2 = f2_pack(sl2, sl2);
-        const uint64_t negx2 = f2_pack(neg, neg);
-        uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {  // keys c*32 + 4i .. +3 -> one TMEM column
-            const int e = c * 32 + 4 * i;
-            float p[4];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const uint64_t xx = f2_fma(f2_pack(WAN_S(e + 2 * u), WAN_S(e + 2 * u + 1)), sl2x2, negx2);
-              float x0, x1;
-              f2_unpack(xx, x0, x1);
-              p[2 * u] = ex2_approx(x0);
-              p[2 * u + 1] = ex2_approx(x1);
-              acc[u] = f2_add(acc[u], f2_pack(p[2 * u], p[2 * u + 1]));
-            }
-            pk[i] = pack_e4m3x4(p[0], p[1], p[2], p[3]);
-          }
-          tmem_st8(tS + c * 8, pk);
-        }
-        float a0, a1, a2, a3;
-        f2_unpack(acc[0], a0, a1);
-        f2_unpack(acc[1], a2, a3);
 #undef WAN_S
-        l += (a0 + a1) + (a2 + a3);
+        l += tsum;
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();

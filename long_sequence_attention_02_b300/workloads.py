@@ -53,6 +53,10 @@ WORKLOADS = {
     # The same 75,600-token, 40-head forward computed in FP8 (e4m3).
     "wan14b_720p_self_fwd_fp8": Workload("wan14b_720p_self_fwd_fp8", "self_fwd_fp8", 1, latent_grid(81, 720, 1280),
                                          40),
+    # The 32,760-token, 12-head forward in FP8: small enough for a full
+    # profiler capture of the FP8 kernel.
+    "wan1.3b_480p_self_fwd_fp8": Workload("wan1.3b_480p_self_fwd_fp8", "self_fwd_fp8", 1, latent_grid(81, 480, 832),
+                                          12),
     "train_64x64x64_fwd_bwd": Workload("train_64x64x64_fwd_bwd", "self_fwd_bwd", 1, (64, 64, 64), 12),
     # Same step at 1/64 of the size (32,768 tokens): small enough for a full
     # profiler capture of the backward kernel.

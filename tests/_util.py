@@ -53,3 +53,44 @@ def compare(got, ref, name, max_abs=MAX_ABS, rel_l2=REL_L2):
 
 def scale_of(d=128):
     return 1.0 / math.sqrt(d)
+
+
+def bf16_round(x):
+    """bf16 bits of float values, rounded to nearest even (finite inputs)."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def rows_whose_reference_moves(qf, kf, grid, bound=256.0):
+    """How many query rows of a self-attention forward move their softmax
+    reference at least once, following the kernels' schedule: an item is 256
+    query rows of one (b, h); it visits its 128-key tiles cyclically from tile
+    qp * n_tiles // n_qpairs; the first tile visited sets the reference to its
+    row maximum, and a later tile whose row sum of 2^(x - m) exceeds `bound`
+    moves it to that tile's maximum. Lets a test check that its inputs really
+    take that path."""
+    from oracle import ref
+
+    B, L, H, d = qf.shape
+    ang = ref.rope_angles(*grid, d)
+    n_tiles = (L + 127) // 128
+    n_qpairs = (L + 255) // 256
+    c = scale_of(d) * math.log2(math.e)
+    moved_rows = 0
+    for b in range(B):
+        for h in range(H):
+            x = (ref.rope_rotate(qf[b, :, h], ang) @ ref.rope_rotate(kf[b, :, h], ang).T) * c
+            for qp in range(n_qpairs):
+                xs = x[256 * qp:256 * (qp + 1)]
+                start = qp * n_tiles // n_qpairs
+                order = [(start + j) % n_tiles for j in range(n_tiles)]
+                m = xs[:, 128 * order[0]:128 * (order[0] + 1)].max(axis=1)
+                moved = np.zeros(len(xs), dtype=bool)
+                for t in order[1:]:
+                    blk = xs[:, 128 * t:128 * (t + 1)]
+                    need = np.exp2(blk - m[:, None]).sum(axis=1) > bound
+                    m = np.where(need, np.maximum(m, blk.max(axis=1)), m)
+                    moved |= need
+                moved_rows += int(moved.sum())
+    return moved_rows

@@ -22,7 +22,7 @@ import pytest
 import long_sequence_attention_02_b300 as wan
 from long_sequence_attention_02_b300 import synth
 from oracle import ref
-from tests._util import bits, compare, dev_to_f64, f64, to_dev
+from tests._util import bf16_round, bits, compare, dev_to_f64, f64, rows_whose_reference_moves, to_dev
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -73,6 +73,22 @@ def test_fp8_zero_queries_give_mean_values():
     mean_v = np.broadcast_to(mean_v, o.shape)
     compare(o, mean_v, "O(Q=0, fp8)", max_abs=FP8_MAX_ABS_FRACTION * float(np.abs(mean_v).max()), rel_l2=FP8_REL_L2)
     np.testing.assert_allclose(lse, math.log(256), atol=1e-4)
+
+
+def test_fp8_reference_moves():
+    """Keys of the first 8 of 16 key tiles scaled by 1/16 and the rest by 1.5:
+    items that start in the small half move their softmax reference at the
+    first large tile (row sums of P above the bound), rescale O and l and
+    recompute that tile. The larger logits stay within the derived tolerance
+    (logit error ~0.05 per unit of logit spread)."""
+    B, grid, H = 1, (8, 16, 16), 2
+    L = 2048
+    qb, kb, vb = _inputs(B, grid, H, seed=54)
+    kb = bf16_round(f64(kb) * np.where(np.arange(L) // 128 < 8, 0.0625, 1.5)[None, :, None, None])
+    assert rows_whose_reference_moves(f64(qb), f64(kb), grid) > 300
+    o, lse = _run(qb, kb, vb, grid)
+    o_ref, lse_ref = ref.self_attention_fwd(f64(qb), f64(kb), f64(vb), grid)
+    compare_fp8(o, o_ref, lse, lse_ref, "fp8, moving reference")
 
 
 def test_fp8_tracks_the_bf16_path():

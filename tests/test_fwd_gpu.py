@@ -11,7 +11,7 @@ import pytest
 import long_sequence_attention_02_b300 as wan
 from long_sequence_attention_02_b300 import synth
 from oracle import ref
-from tests._util import MAX_ABS, REL_L2, bits, compare, dev_to_f64, f64, to_dev
+from tests._util import MAX_ABS, REL_L2, bits, bf16_round, compare, dev_to_f64, f64, rows_whose_reference_moves, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -117,6 +117,24 @@ def test_self_attention_one_hot_logit():
     compare(o, o_ref, "O")
     compare(lse, lse_ref, "LSE")
     assert np.abs(o[0, i0, 0] - f64(vb)[0, i0, 0]).max() < 0.05
+
+
+def test_self_attention_reference_moves():
+    """Keys of the first 8 of 16 key tiles scaled by 1/8 and the rest by 2
+    (exact in bf16). An item that starts in the small half takes its softmax
+    reference there, and the first large tile's row sums exceed the bound, so
+    those rows rescale O and l and recompute the tile."""
+    B, grid, H = 1, (8, 16, 16), 2
+    L = 2048
+    qb, kb, vb = _self_inputs(B, grid, H, seed=13)
+    kf = f64(kb) * np.where(np.arange(L) // 128 < 8, 0.125, 2.0)[None, :, None, None]
+    kb = bf16_round(kf)
+    assert np.array_equal(f64(kb), kf)
+    assert rows_whose_reference_moves(f64(qb), kf, grid) > 1000
+    o, lse = _run_self(qb, kb, vb, grid)
+    o_ref, lse_ref = ref.self_attention_fwd(f64(qb), kf, f64(vb), grid)
+    compare(o, o_ref, "O")
+    compare(lse, lse_ref, "LSE")
 
 
 def _run_cross(qb, kb, vb, lens, grid):
