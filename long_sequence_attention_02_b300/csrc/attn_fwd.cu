@@ -18,7 +18,7 @@
 //   warp  8     TMA producer of K_j, V_j (ring)
 //   warp  9     MMA issuer (warp-converged, one elected lane) and TMEM owner
 //   warp  10    TMA producer of the items' Q tiles
-//   warp  11    idle                                               72 regs
+//   warp  11    O store: TMA stores of the staged O tiles, Q buffer release  72 regs
 // Cross-attention items are short (at most 4 key tiles), so there Q is
 // double-buffered: the next item's Q load and first QK overlap the current
 // item's output epilogue. Self-attention uses one Q buffer and a 4-slot ring.
@@ -58,6 +58,7 @@ constexpr uint32_t kControlRegs = 72;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kQLoadWarp = 10;
+constexpr int kStoreWarp = 11;
 // Q buffers and K/V ring slots (self-attention: 1 + 4, cross-attention: 2 + 3).
 template <bool kRope>
 struct FwdCfg {
@@ -139,9 +140,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t bar_s_full[kQTiles], bar_p_full[kQTiles], bar_o_full[kQTiles];
   __shared__ __align__(8) uint64_t bar_drain;
   __shared__ __align__(8) uint64_t bar_oldo[kQTiles];  // previous O tile loaded (merging epilogues)
+  // O tile t of the item in Q buffer q written to its staging area. One
+  // barrier per buffer: its next phase needs that buffer's next Q load,
+  // which waits for the store warp to have consumed this one.
+  __shared__ __align__(8) uint64_t bar_o_staged[kQBuf][kQTiles];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   __shared__ int epi_ok[kQTiles][4];  // per-warp epilogue go/stop flags
+  __shared__ int store_ok[kQBuf][kQTiles];  // staged O tile is valid (read by the store warp)
   // The first key lengths, read once per CTA instead of at every item.
   constexpr int kLensCached = 64;
   __shared__ int lens_sh[kLensCached];
@@ -183,7 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int q = 0; q < kQBuf; ++q) {
       mbar_init(&bar_q_full[q], 1);
       mbar_init(&bar_q_ready[q], kRope ? 8 : 1);
-      mbar_init(&bar_q_empty[q], kQTiles);  // one arrive per query tile, after its O store
+      mbar_init(&bar_q_empty[q], 1);  // the store warp, once both O tiles' stores have read it
+      for (int t = 0; t < kQTiles; ++t) mbar_init(&bar_o_staged[q][t], 4);
     }
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(&bar_s_full[t], 1);
@@ -355,6 +362,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit_elect(&bar_drain);
       mbar_wait(&bar_drain, 0, nullptr, to);
     }
+   } else if (warp == kStoreWarp) {
+    // ------------------------------------------------------------ O store
+    // Writes each staged O tile with two TMA tensor stores and, once both
+    // tiles' stores have read the staging area, hands the Q buffer back to
+    // the Q producer. The softmax warps go on to their next item as soon as
+    // their tile is staged. Rows past the end of the sequence fall outside
+    // the tensor map and are not written.
+    if (lane == 0) {
+      int nq = 0;
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const Item x = item_of(it);
+        if (x.n_tiles == 0) continue;
+        const int qb = nq % kQBuf;
+        bool ok = true;
+        for (int t = 0; t < kQTiles && ok; ++t) {
+          ok = mbar_wait(&bar_o_staged[qb][t], (nq / kQBuf) & 1, abort, to);
+          if (ok && store_ok[qb][t]) {
+            uint8_t* stage = sQ + (qb * kQTiles + t) * kTileBytes;
+            tma_store_4d(&tm_o, stage, 0, x.h, x.q0 + t * kBlockM, x.b);
+            tma_store_4d(&tm_o, stage + kHalfBytes, 64, x.h, x.q0 + t * kBlockM, x.b);
+            bulk_commit_group();
+          }
+        }
+        if (!ok) {
+          raise_abort(abort, a.lc.err);
+          break;
+        }
+        bulk_wait_group_read0();
+        mbar_arrive(&bar_q_empty[qb]);
+        ++nq;
+      }
+      bulk_wait_group0();
+    }
+    __syncwarp();
    }
   } else {
     regs_grow<kSoftmaxRegs>();
@@ -499,10 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---------------------------------------------------------- epilogue
       // O_t is normalised into bf16 and staged in this tile's Q buffer (no
-      // MMA reads it once O_t is final) in the 128-byte swizzled layout, then
-      // one thread writes it with two TMA tensor stores and, once they have
-      // read the staging area, hands the buffer back to the Q producer. The
-      // four warps of the tile agree on stopping before the named barriers.
+      // MMA reads it once O_t is final) in the 128-byte swizzled layout; the
+      // store warp writes it out and hands the buffer back to the Q
+      // producer. The four warps of the tile agree on stopping before the
+      // named barrier.
       if (ok) ok = warp_wait(&bar_o_full[t], nq & 1, abort, a.lc.err, to);
       if (lane == 0) epi_ok[t][wq] = ok ? 1 : 0;
       named_bar_sync(1 + t, 128);
@@ -572,24 +613,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           a.lse[(static_cast<size_t>(x.b) * a.H + x.h) * a.Lq + row] = lse_out;
         fence_proxy_async_smem();
       }
-      named_bar_sync(1 + t, 128);
-      if (all_ok && wq == 0 && lane == 0) {
-        // Rows past the end of the sequence fall outside the tensor map and
-        // are not written.
-        tma_store_4d(&tm_o, stage, 0, x.h, x.q0 + t * kBlockM, x.b);
-        tma_store_4d(&tm_o, stage + kHalfBytes, 64, x.h, x.q0 + t * kBlockM, x.b);
-        bulk_commit_group();
-        bulk_wait_group_read0();
-        mbar_arrive(&bar_q_empty[qb]);
-      }
+      // The store warp writes the staged tile out (store_ok[qb][t] is next
+      // written for the item after the store warp has released buffer qb).
+      if (wq == 0 && lane == 0) store_ok[qb][t] = all_ok ? 1 : 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_o_staged[qb][t]);
       sp += n_tiles;
       ++nq;
     }
   }
 
-  // The O stores still in flight finish before the kernel's writes become
-  // visible; only their reads of shared memory must end before exit.
-  if (warp == 0 || warp == 4) bulk_wait_group0();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
