@@ -108,7 +108,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 __device__ __forceinline__ void load32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   tmem_ld32(taddr, r);
-  tmem_ld_wait();
+  tmem_ld_wait_regs(r);
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t v[64];
       tmem_ld32(tS + lane_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
       tmem_ld32(tS + lane_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-      tmem_ld_wait();
+      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[64]>(&v[0]));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarDQFree0]);
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (half == 0) {
           tmem_ld32(tDP + lane_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
           tmem_ld32(tDP + lane_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-          tmem_ld_wait();
+          tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[64]>(&v[0]));
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[kBarDQFree1]);

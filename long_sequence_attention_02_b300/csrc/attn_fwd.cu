@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sr[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
-        tmem_ld_wait();
+        tmem_ld_wait_regs(sr);
 #define WAN_S(e) __uint_as_float(sr[(e) >> 5][(e) & 31])
         const int jt = j + kv_start < n_tiles ? j + kv_start : j + kv_start - n_tiles;
         const int valid = n_valid - jt * kBlockN;
@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 4; ++c) {
             uint32_t ov[32];
             tmem_ld32(tO + c * 32, ov);
-            tmem_ld_wait();
+            tmem_ld_wait_regs(ov);
 #pragma unroll
             for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
             tmem_st32(tO + c * 32, ov);
@@ -588,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) {
           uint32_t ov[32];
           tmem_ld32(tO + c * 32, ov);
-          tmem_ld_wait();
+          tmem_ld_wait_regs(ov);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {  // 16-byte chunk 4c+q of the row: half c/2, chunk (4c+q)%8
             const int chunk = 4 * c + q;

@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
         uint32_t sr[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr[c]);
-        tmem_ld_wait();
+        tmem_ld_wait_regs(sr);
 #define WAN_S(e) __uint_as_float(sr[(e) >> 5][(e) & 31])
         const int jt = j + kv_start < n_tiles ? j + kv_start : j + kv_start - n_tiles;
         if (jt == n_tiles - 1 && valid_last < kTile) {
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
           for (int c = 0; c < 4; ++c) {
             uint32_t ov[32];
             tmem_ld32(tO + c * 32, ov);
-            tmem_ld_wait();
+            tmem_ld_wait_regs(ov);
 #pragma unroll
             for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
             tmem_st32(tO + c * 32, ov);
@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
           for (int c = 0; c < 2; ++c) {
             uint32_t ov[32];
             tmem_ld32(tO + half * 64 + c * 32, ov);
-            tmem_ld_wait();
+            tmem_ld_wait_regs(ov);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int chunk = 4 * c + q;  // 16-byte chunk of the 64-column half row

@@ -322,7 +322,26 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 #undef WAN_R8
 #undef WAN_W8
 
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// tcgen05.wait::ld naming, as in-out operands, the registers that the
+// preceding tcgen05.ld instructions write. Those loads fill their registers
+// asynchronously and the registers are undefined until the wait; tying them
+// to the wait keeps the compiler from reading or copying them before it.
+#define WAN_TIE4(a, i) "+r"(a[(i)]), "+r"(a[(i) + 1]), "+r"(a[(i) + 2]), "+r"(a[(i) + 3])
+#define WAN_TIE16(a, i) WAN_TIE4(a, i), WAN_TIE4(a, (i) + 4), WAN_TIE4(a, (i) + 8), WAN_TIE4(a, (i) + 12)
+#define WAN_TIE32(a, i) WAN_TIE16(a, i), WAN_TIE16(a, (i) + 16)
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : WAN_TIE32(r, 0)::"memory");
+}
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[64]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : WAN_TIE32(r, 0), WAN_TIE32(r, 32)::"memory");
+}
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[4][32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : WAN_TIE32(r[0], 0), WAN_TIE32(r[1], 0), WAN_TIE32(r[2], 0), WAN_TIE32(r[3], 0)::"memory");
+}
+#undef WAN_TIE32
+#undef WAN_TIE16
+#undef WAN_TIE4
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
