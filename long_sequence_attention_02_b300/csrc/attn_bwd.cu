@@ -19,7 +19,9 @@
 //        dS^T = scale * P^T o (dP^T - D)                (threads, into TMEM + smem)
 //        dK  += dS^T Q_rot                              (A = dS^T from TMEM)
 //        dQ_i = dS K_rot  (two N=64 halves)             (A = dS from smem, MN-major)
-//      and the threads add dQ_i into the fp32 accumulator with vector atomics.
+//      The dQ warpgroup reads dQ_i out of TMEM, stages it in the dS buffer
+//      (once the dQ MMA has read dS) as 128B-swizzled 128 x 32-float boxes,
+//      and adds it into the fp32 accumulator with bulk tensor reductions.
 //      TMEM: dV [0,128) dK [128,256) S [256,384) dP [384,512); P^T, dS^T
 //      (bf16) and the dQ halves reuse S and dP columns once the MMAs that read
 //      them are ordered before (tcgen05 MMAs of one thread run in order).
