@@ -131,3 +131,61 @@ def test_debug_hook_argument_checks(lib):
     assert wan.wan_debug_inject_stall(-1, 10) == wan.WAN_ERR_INVALID
     assert wan.wan_debug_inject_stall(1, 0) == wan.WAN_ERR_INVALID
     assert wan.wan_debug_inject_stall(0, 100) == wan.WAN_OK
+
+
+def test_fp8_workspace_size(lib):
+    # e4m3 Q and K [B, L, H, 128], V transposed to [B, H, 128, Lpad] (Lpad = L rounded up to 16)
+    # and the per-head amax triples, each region 256-byte aligned
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    for B, g, H in [(1, (21, 45, 80), 40), (2, (3, 7, 9), 3), (1, (1, 1, 1), 1)]:
+        L = g[0] * g[1] * g[2]
+        lpad = (L + 15) // 16 * 16
+        n = B * L * H * 128
+        want = up(n) + up(n) + up(B * H * 128 * lpad) + up(B * H * 3 * 4)
+        assert wan.wan_attn_workspace_size(wan.WAN_OP_FWD_FP8, B, g, H) == want
+
+
+def test_fp8_rejects_bad_arguments(lib):
+    g = (2, 4, 4)
+    ws = wan.wan_attn_workspace_size(wan.WAN_OP_FWD_FP8, 1, g, 2)
+    ok = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, grid=g, H=2, head_dim=128, tables=FAKE,
+              scale=0.088, workspace=FAKE, ws_bytes=ws, stream=0)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return wan.wan_attn_fwd_fp8(**a)
+
+    assert call(k=None) == wan.WAN_ERR_INVALID
+    assert call(workspace=None) == wan.WAN_ERR_INVALID
+    assert call(v=FAKE + 4) == wan.WAN_ERR_INVALID
+    assert call(lse=FAKE + 2) == wan.WAN_ERR_INVALID
+    assert call(ws_bytes=ws - 1) == wan.WAN_ERR_INVALID
+    assert call(grid=(2, 0, 4)) == wan.WAN_ERR_INVALID
+    assert call(scale=float("inf")) == wan.WAN_ERR_INVALID
+    assert call(head_dim=256) == wan.WAN_ERR_UNSUPPORTED
+    assert call(B=0, q=None, k=None, v=None, o=None, lse=None, workspace=None, ws_bytes=0) == wan.WAN_OK
+
+
+def test_ring_step_rejects_bad_ranges(lib):
+    g = (2, 4, 4)  # 32 tokens
+    ok = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, grid=g, H=1, head_dim=128, tables=FAKE, scale=0.088,
+              q_start=0, q_len=4, kv_start=0, kv_len=4, accumulate=0, workspace=FAKE, ws_bytes=1 << 16, stream=0)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return wan.wan_attn_fwd_ring_step(**a)
+
+    for bad in [dict(q_start=-1), dict(q_len=0), dict(q_start=30, q_len=3), dict(kv_start=29, kv_len=4),
+                dict(kv_len=0), dict(accumulate=2), dict(lse=None), dict(ws_bytes=4 * 256 - 1)]:
+        assert call(**bad) == wan.WAN_ERR_INVALID, bad
+
+
+def test_noalloc_rejects_problems_larger_than_its_scratch(lib):
+    # one row-head more than the fixed scratch holds fails before any device work
+    assert wan.NOALLOC_MAX_ROW_HEADS == 262144
+    g = (1, 1, 2049)  # 2049 tokens x 128 heads = 262,272 row-heads
+    assert wan.wan_attn_fwd_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 1, g, 128, 128, FAKE, 0.088) == wan.WAN_ERR_INVALID
+    assert wan.wan_attn_fwd_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 1, (0, 4, 4), 2, 128, FAKE, 0.088) == \
+        wan.WAN_ERR_INVALID

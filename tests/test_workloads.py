@@ -29,6 +29,12 @@ def test_named_workloads():
     assert w["train_64x64x64_fwd_bwd"].L == 262144
     assert w["tiny_3x8x8_h2"].L == 192
     assert w["wan14b_720p_self_fwd"].flops() == pytest.approx(1.1705e14, rel=1e-4)
+    # the FP8 workloads are the same problems computed in e4m3
+    for name, base in [("wan14b_720p_self_fwd_fp8", "wan14b_720p_self_fwd"),
+                       ("wan1.3b_480p_self_fwd_fp8", "wan1.3b_480p_self_fwd")]:
+        assert w[name].kind == "self_fwd_fp8"
+        assert (w[name].B, w[name].grid, w[name].H) == (w[base].B, w[base].grid, w[base].H)
+        assert w[name].flops() == w[base].flops()
 
 
 def test_bad_video_shapes():
