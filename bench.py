@@ -171,7 +171,42 @@ class Case:
     moves the step's inputs and results through pinned host memory."""
 
 
+def make_conv_case(wan, torch, dev, w, rank):
+    """One causal Conv3d layer of the VAE on a chunk with its 2-frame cache."""
+    B, T, H, W, ci, co = w.B, w.T, w.H, w.W, w.c_in, w.c_out
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + rank)
+    stream = torch.cuda.current_stream(dev)
+    c = Case()
+    c.stream = stream
+    x = torch.randn(B, T, H, W, ci, device=dev, generator=gen).bfloat16()
+    cache = torch.randn(B, 2, H, W, ci, device=dev, generator=gen).bfloat16()
+    wt = (torch.randn(co, 3, 3, 3, ci, device=dev, generator=gen) / math.sqrt(27 * ci)).bfloat16()
+    bias = torch.randn(co, device=dev, generator=gen) * 0.1
+    y = torch.empty(B, T, H, W, co, dtype=torch.bfloat16, device=dev)
+    cache_out = torch.empty_like(cache)
+
+    def run():
+        wan.check(wan.wan_vae_causal_conv3d(x, cache, wt, bias, y, cache_out, B, T, H, W, ci, co, stream))
+
+    c.inputs, c.outputs = [x, cache, wt, bias], [y, cache_out]
+    c.flops = c.kernel_flops = w.flops()
+    c.kernel, c.launches, c.hbm_bytes, c.bound = "causal_conv3d_kernel", 1, None, "tensor"
+
+    def step(prof=None):
+        if prof is not None:
+            wan.check(wan.wan_profile_set_events(*prof))
+        run()
+
+    c.step = step
+    c.in_bytes = sum(t.numel() * t.element_size() for t in c.inputs)
+    c.out_bytes = sum(t.numel() * t.element_size() for t in c.outputs)
+    return c
+
+
 def make_case(wan, torch, dev, w, rank, peaks):
+    if w.kind == "conv3d":
+        return make_conv_case(wan, torch, dev, w, rank)
     B, L, H, d, grid = w.B, w.L, w.H, w.d, w.grid
     scale = 1.0 / math.sqrt(d)
     gen = torch.Generator(device=dev)
@@ -288,12 +323,12 @@ def run_ours(args, rank, world, local):
     import torch
 
     import long_sequence_attention_02_b300 as wan
-    from long_sequence_attention_02_b300.workloads import WORKLOADS
+    from long_sequence_attention_02_b300.workloads import CONV_WORKLOADS, WORKLOADS
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks = _peaks()
-    w = WORKLOADS[args.workload]
+    w = WORKLOADS[args.workload] if args.workload in WORKLOADS else CONV_WORKLOADS[args.workload]
     c = make_case(wan, torch, dev, w, rank, peaks)
     stream = c.stream
 
@@ -378,11 +413,18 @@ def run_ours(args, rank, world, local):
                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": f"HBM copy ({peaks['source']})",
                     "algorithmic_bytes": c.hbm_bytes, "kernel_ms": round(kernel_ms, 3), "traffic": traffic,
                     "tensor_tflops_nominal": round(c.kernel_flops / (kernel_ms / 1e3) / 1e12, 2)}
-    config = {"workload": w.name, "kind": w.kind, "B": w.B, "grid": list(w.grid), "tokens": w.L, "heads": w.H,
-              "head_dim": w.d, "flop_per_step": c.flops,
-              "l2": f"inputs {c.in_bytes / 2**30:.2f} GiB > L2 126 MB (no flush needed)",
-              "frac_of_2.25PF_spec": round(value / 2250.0, 4)}
-    if w.kind != "cross_fwd":
+    if w.kind == "conv3d":
+        config = {"workload": w.name, "kind": w.kind, "B": w.B, "frames": w.T, "height": w.H, "width": w.W,
+                  "c_in": w.c_in, "c_out": w.c_out, "kernel": [3, 3, 3],
+                  "cache": "2 frames of the previous chunk, written for the next one", "flop_per_step": c.flops,
+                  "l2": f"input x {c.inputs[0].numel() * 2 / 2**20:.0f} MiB > L2 126 MB (no flush needed)",
+                  "frac_of_2.25PF_spec": round(value / 2250.0, 4)}
+    else:
+        config = {"workload": w.name, "kind": w.kind, "B": w.B, "grid": list(w.grid), "tokens": w.L, "heads": w.H,
+                  "head_dim": w.d, "flop_per_step": c.flops,
+                  "l2": f"inputs {c.in_bytes / 2**30:.2f} GiB > L2 126 MB (no flush needed)",
+                  "frac_of_2.25PF_spec": round(value / 2250.0, 4)}
+    if w.kind not in ("cross_fwd", "conv3d"):
         config["theta"] = 10000.0
     config.update(getattr(c, "extra_config", {}))
     line = {
@@ -447,6 +489,11 @@ def extras(wan, torch, dev, peaks, skip=None):
     w = WORKLOADS["train_64x64x64_fwd_bwd"]
     if w.name != skip:
         _extra_train(wan, torch, dev, w, stream, timeit, out)
+    from long_sequence_attention_02_b300.workloads import CONV_WORKLOADS
+
+    w = CONV_WORKLOADS["wan_vae_conv3d_360x640_192"]
+    if w.name != skip:
+        _extra_conv(wan, torch, dev, w, stream, timeit, out, peaks)
     return out
 
 
@@ -529,6 +576,15 @@ def _extra_train(wan, torch, dev, w, stream, timeit, out):
                    "tflops_step": round(3.5 * ffl / tot / 1e9, 1)}
 
 
+def _extra_conv(wan, torch, dev, w, stream, timeit, out, peaks):
+    c = make_conv_case(wan, torch, dev, w, 0)
+    tot, ker = timeit(lambda p: c.step(p), iters=5, prof=True)
+    out[w.name] = {"ms": round(tot, 3), "tflops": round(w.flops() / tot / 1e9, 1),
+                   "kernel_tflops": round(w.flops() / ker / 1e9, 1),
+                   "kernel_frac_of_bf16_sustained": round(w.flops() / ker / 1e9 / peaks["bf16_tflops_sustained"], 4)}
+    del c
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline leg and reference arm)
 
@@ -538,6 +594,7 @@ KERNEL_SOURCES = {
     "attn_fwd_kernel<false>": ("attn_fwd.cu", "common.cuh"),
     "attn_bwd_kernel": ("attn_bwd.cu", "common.cuh"),
     "attn_fwd_fp8_kernel": ("attn_fwd_fp8.cu", "common.cuh"),
+    "causal_conv3d_kernel": ("conv3d.cu", "common.cuh"),
 }
 
 
@@ -587,7 +644,33 @@ def _oracle_rows(w, rows_per_head: int, heads: int, seed: int = 0):
     return n, dt, per_row
 
 
+def _oracle_conv(w, n_pos: int, seed: int = 0):
+    """Time the conv oracle on n_pos output positions, each computed from its
+    3 x 3 x 3 window (drawn from the seeded generator) against all C_out.
+    Returns (positions, seconds, FLOP per position)."""
+    import numpy as np
+
+    from long_sequence_attention_02_b300 import synth
+    from oracle import vae
+
+    ci, co = w.c_in, w.c_out
+    wt = synth.bf16_bits_to_f64(synth.normal_bf16(seed, synth.STREAM_V, (co, 3, 3, 3, ci))) / math.sqrt(27 * ci)
+    rng = np.random.default_rng(seed)
+    t0 = time.perf_counter()
+    for i in range(n_pos):
+        off = int(rng.integers(0, 2**40)) * 27 * ci
+        win = synth.bf16_bits_to_f64(synth.normal_bf16(seed, synth.STREAM_Q, (1, 3, 3, 3, ci), offset=off))
+        vae.causal_conv3d_at(win, wt, None, None, [(0, 2, 1, 1)])
+    dt = time.perf_counter() - t0
+    return n_pos, dt, 2.0 * 27 * ci * co
+
+
 def cpu_baseline(w, rows_per_head: int):
+    if w.kind == "conv3d":
+        n, dt, per = _oracle_conv(w, 2 * rows_per_head)
+        return {"value": round(per * n / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                "sample": f"{n} output positions of {w.name}, each from its 3x3x3 window against all {w.c_out} "
+                          f"output channels, fp64 numpy, {dt:.1f} s", "positions_per_s": round(n / dt, 1)}
     n, dt, per_row = _oracle_rows(w, rows_per_head, heads=2)
     what = {"self_fwd": "forward", "self_fwd_fp8": "forward", "cross_fwd": "cross-attention forward",
             "self_fwd_bwd": "forward + dQ backward"}[w.kind]
@@ -601,6 +684,8 @@ def run_reference(args, rank, world):
 
     if rank != 0:
         return
+    if args.workload not in WORKLOADS:
+        return run_reference_conv(args, world)
     w = WORKLOADS[args.workload]
     rows = args.ref_rows
     for _ in range(args.warmup):
@@ -623,6 +708,33 @@ def run_reference(args, rank, world):
                    "head_dim": w.d},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_conv(args, world):
+    from long_sequence_attention_02_b300.workloads import CONV_WORKLOADS
+
+    w = CONV_WORKLOADS[args.workload]
+    n = 4 * args.ref_rows
+    for _ in range(args.warmup):
+        _oracle_conv(w, n)
+    dt, fl = 0.0, 0.0
+    for _ in range(args.steps):
+        k, t, per = _oracle_conv(w, n)
+        dt += t
+        fl += per * k
+    value = fl / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: bf16 N(0,1) from the seeded SplitMix64 generator",
+        "config": {"workload": w.name, "kind": w.kind, "B": w.B, "frames": w.T, "height": w.H, "width": w.W,
+                   "c_in": w.c_in, "c_out": w.c_out},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{n} output positions per step, each from its 3x3x3 window (fp64 numpy oracle)"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -255,6 +255,35 @@ int wan_debug_inject_stall(int count, int timeout_ms);
 int wan_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g,
                          int H, int head_dim, const float* tables, float scale, void* stream);
 
+/*
+ * One causal 3D convolution layer of the Wan-VAE on one chunk of frames, with
+ * its feature cache (gojay.top "Wan2.1" reading, Feature Cache section and
+ * Fig. vae_cache (a): a time kernel of 3 reads frames t-2, t-1 and t; the
+ * first chunk is padded with two zero frames in time, every later chunk is
+ * prefixed with the previous chunk's last two input frames, so that chunked
+ * processing equals one convolution over the whole video).
+ *
+ *   y[b,t,h,w,o] = bias[o] + sum_{kt,kh,kw,c} weight[o,kt,kh,kw,c] * xp[b, t+kt, h+kh-1, w+kw-1, c]
+ *
+ * with xp = (cache, or two zero frames) ++ x in time and zero outside the
+ * picture (a cross-correlation, stride 1, 3 x 3 x 3 kernel).
+ *   x         : [B, T, H, W, c_in]  bf16, channels last (device)
+ *   cache     : [B, 2, H, W, c_in]  bf16, the previous chunk's last two input frames,
+ *               or NULL for a first chunk (zeros)
+ *   weight    : [c_out, 3, 3, 3, c_in] bf16
+ *   bias      : [c_out] fp32, or NULL
+ *   y         : [B, T, H, W, c_out] bf16 (output; must not overlap the inputs)
+ *   cache_out : [B, 2, H, W, c_in] bf16, receives the last two frames of
+ *               (cache or zeros) ++ x for the next chunk; may be NULL, and may
+ *               be the same buffer as cache (it is written after the
+ *               convolution has read cache, in stream order)
+ * c_in and c_out must be multiples of 64 (WAN_ERR_UNSUPPORTED otherwise);
+ * bf16 pointers 16-byte aligned, bias 4-byte aligned. B = 0 is a no-op.
+ * The reduction is accumulated in fp32 on tensor cores; y is rounded to bf16.
+ */
+int wan_vae_causal_conv3d(const void* x, const void* cache, const void* weight, const float* bias, void* y,
+                          void* cache_out, int B, int T, int H, int W, int c_in, int c_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

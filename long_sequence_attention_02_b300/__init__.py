@@ -34,7 +34,7 @@ EXPORTED = (
     "wan_status_str", "wan_version", "wan_rope3d_tables_size", "wan_rope3d_tables",
     "wan_attn_workspace_size", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
     "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall", "wan_attn_fwd_noalloc",
-    "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual", "wan_attn_fwd_fp8",
+    "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual", "wan_attn_fwd_fp8", "wan_vae_causal_conv3d",
 )
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 NOALLOC_MAX_ROW_HEADS = NOALLOC_SCRATCH_BYTES // 256
@@ -78,12 +78,14 @@ def load_library(path: str = LIB_PATH):
                                            i32, i32, vp, sz, vp]
     lib.wan_xattn_fwd_dual.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, vp, i32, wan_grid_t, i32, i32,
                                        f32, vp]
+    lib.wan_vae_causal_conv3d.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     lib.wan_get_device_status.argtypes = [vp]
     lib.wan_debug_inject_stall.argtypes = [i32, i32]
     lib.wan_profile_set_events.argtypes = [vp, vp]
     for name in ("wan_rope3d_tables", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
                  "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall",
-                 "wan_attn_fwd_noalloc", "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual", "wan_attn_fwd_fp8"):
+                 "wan_attn_fwd_noalloc", "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual", "wan_attn_fwd_fp8",
+                 "wan_vae_causal_conv3d"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -173,6 +175,11 @@ def wan_attn_fwd_fp8(q, k, v, o, lse, B, grid, H, head_dim, tables, scale, works
     return load_library().wan_attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, _grid(grid), H,
                                             head_dim, _ptr(tables), float(scale), _ptr(workspace), int(ws_bytes),
                                             _stream(stream))
+
+
+def wan_vae_causal_conv3d(x, cache, weight, bias, y, cache_out, B, T, H, W, c_in, c_out, stream=None) -> int:
+    return load_library().wan_vae_causal_conv3d(_ptr(x), _ptr(cache), _ptr(weight), _ptr(bias), _ptr(y),
+                                                 _ptr(cache_out), B, T, H, W, c_in, c_out, _stream(stream))
 
 
 def wan_attn_fwd_ring_step(q, k, v, o, lse, B, grid, H, head_dim, tables, scale, q_start, q_len, kv_start, kv_len,
@@ -286,3 +293,22 @@ def attention_backward(q, k, v, o, lse, dout, grid, tables=None, scale=None, the
     check(wan_attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, grid, H, d, tables, scale, ws, ws_bytes, stream),
           "wan_attn_bwd")
     return dq, dk, dv
+
+
+def causal_conv3d(x, weight, bias=None, cache=None, stream=None):
+    """One causal 3x3x3 Conv3d layer of the Wan-VAE on one chunk of frames.
+
+    x: bf16 [B, T, H, W, C_in] on the GPU; weight: bf16 [C_out, 3, 3, 3, C_in];
+    bias: fp32 [C_out] or None; cache: bf16 [B, 2, H, W, C_in] from the previous
+    chunk, or None for a first chunk. Returns (y [B, T, H, W, C_out], the cache
+    for the next chunk).
+    """
+    import torch
+
+    B, T, H, W, c_in = x.shape
+    c_out = weight.shape[0]
+    y = torch.empty(B, T, H, W, c_out, dtype=torch.bfloat16, device=x.device)
+    new_cache = torch.empty(B, 2, H, W, c_in, dtype=torch.bfloat16, device=x.device)
+    check(wan_vae_causal_conv3d(x, cache, weight, bias, y, new_cache, B, T, H, W, c_in, c_out, stream),
+          "wan_vae_causal_conv3d")
+    return y, new_cache

@@ -1,0 +1,294 @@
+// Causal 3 x 3 x 3 Conv3d of the Wan-VAE with its feature cache, for sm_103a:
+// an implicit GEMM on tcgen05 tensor cores.
+//
+// What is computed (gojay.top "Wan2.1" reading, Feature Cache section and
+// Fig. vae_cache (a)): for one chunk of T frames,
+//   y[b,t,h,w,o] = bias[o] + sum_{kt,kh,kw,c} wt[o,kt,kh,kw,c] * xp[b, t+kt, h+kh-1, w+kw-1, c],
+// where xp is the chunk with its two past frames in front of it in time (the
+// cache, i.e. the previous chunk's last two input frames, or zeros for the
+// first chunk) and zero outside the picture. Activations are channels-last
+// bf16 [B, T, H, W, C]; weights [C_out, 3, 3, 3, C_in] bf16; bias fp32.
+//
+// GEMM view: M = output positions, N = C_out, K = 27 taps x C_in. One CTA
+// computes a tile of 128 positions x N channels: the positions are an 8 (h)
+// x 16 (w) patch of one frame, N the largest of 256, 192, 128 and 64 that
+// divides C_out. Per K step (one tap, 64 input channels):
+// - A = the 128 input pixels that tap reads, 64 channels each: one 5D TMA box
+//   {64 c, 16 w, 8 h, 1 t, 1 b} at the tap's offset. Its zero fill outside
+//   the tensor is the spatial padding, and, for a first chunk, the causal
+//   padding too (a negative frame coordinate). With a cache, taps that reach
+//   before the chunk read the cache tensor instead.
+// - B = the tap's N x 64 weights: one 3D box {64 c, 1 tap, N}.
+// Both land 128B-swizzled (rows of 128 bytes), and four tcgen05.mma of
+// kind::f16 (K = 16 each) accumulate into TMEM.
+//
+// Warps: 0 TMA producer, 1 MMA issuer and TMEM owner, 2-5 epilogue
+// (TMEM -> + bias -> bf16 -> global, positions inside the picture only).
+// Every wait is bounded; on a timeout the device error word is set.
+#include <climits>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace wan {
+
+namespace {
+
+constexpr int kPatchH = 8;
+constexpr int kPatchW = 16;                   // 128 output positions per tile
+constexpr int kChunkC = 64;                   // input channels per K step (128 bytes)
+constexpr int kStagesC = 4;
+constexpr int kATile = 128 * 128;             // 128 rows x 64 bf16
+constexpr int kBTileMax = 256 * 128;          // up to 256 rows x 64 bf16
+constexpr int kStageC = kATile + kBTileMax;   // 48 KB
+constexpr int kConvSmem = kStagesC * kStageC + 1024;
+constexpr int kConvThreads = 192;
+constexpr uint32_t kConvTmemCols = 256;
+
+struct ConvArgs {
+  const float* bias;     // [C_out] or null
+  __nv_bfloat16* y;      // [B, T, H, W, C_out]
+  int B, T, H, W, c_in, c_out, n_tile;
+  int tiles_h, tiles_w;
+  int has_cache;
+  LaunchCommon lc;
+};
+
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                            int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void conv_abort(volatile int* abort, int* err) {
+  *abort = 1;
+  atomicCAS(err, 0, kDevTimeout);
+}
+
+__global__ void __launch_bounds__(kConvThreads, 1)
+    causal_conv3d_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_cache,
+                         const __grid_constant__ CUtensorMap tm_w, const ConvArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  __shared__ __align__(8) uint64_t bar_full[kStagesC], bar_empty[kStagesC], bar_acc;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort = &abort_sh;
+  const uint64_t to = a.lc.timeout_ns;
+
+  // Tile: (b, t, patch row, patch column) from blockIdx.x, channels from blockIdx.y.
+  int m = blockIdx.x;
+  const int tw = m % a.tiles_w;
+  m /= a.tiles_w;
+  const int th = m % a.tiles_h;
+  m /= a.tiles_h;
+  const int t = m % a.T;
+  const int b = m / a.T;
+  const int h0 = th * kPatchH, w0 = tw * kPatchW;
+  const int n0 = blockIdx.y * a.n_tile;
+  const int c_steps = a.c_in / kChunkC;
+  const int k_steps = 27 * c_steps;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesC; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    mbar_init(&bar_acc, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, kConvTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint32_t tx = static_cast<uint32_t>(kATile + a.n_tile * 128);
+      int issued = 0;
+      for (int k = 0; k < k_steps; ++k) {
+        const int slot = k % kStagesC;
+        if (k >= kStagesC && !mbar_wait(&bar_empty[slot], ((k / kStagesC) - 1) & 1, abort, to)) {
+          conv_abort(abort, a.lc.err);
+          break;
+        }
+        const int tap = k / c_steps;
+        const int c0 = (k % c_steps) * kChunkC;
+        const int kt = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
+        const int ti = t + kt - 2;  // input frame of this tap, < 0 before the chunk
+        uint8_t* sa = smem + slot * kStageC;
+        mbar_arrive_expect_tx(&bar_full[slot], tx);
+        if (ti < 0 && a.has_cache)
+          tma_load_5d(sa, &tm_cache, &bar_full[slot], c0, w0 + kw - 1, h0 + kh - 1, ti + 2, b);
+        else  // before a first chunk (ti < 0) the box lies outside x and reads zeros
+          tma_load_5d(sa, &tm_x, &bar_full[slot], c0, w0 + kw - 1, h0 + kh - 1, ti, b);
+        tma_load_3d(sa + kATile, &tm_w, &bar_full[slot], c0, tap, n0);
+        ++issued;
+      }
+      // Every copy this warp issued lands before the CTA may exit.
+      for (int k = issued - kStagesC < 0 ? 0 : issued - kStagesC; k < issued; ++k)
+        mbar_wait(&bar_full[k % kStagesC], (k / kStagesC) & 1, nullptr, to);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(a.n_tile), 0, 0);
+    const uint64_t d0 = sdesc_sw128(smem_u32(smem), 16, 1024);
+    const uint32_t hi = static_cast<uint32_t>(d0 >> 32);
+    const uint32_t lo0 = static_cast<uint32_t>(d0);
+    bool ok = true;
+    for (int k = 0; k < k_steps && ok; ++k) {
+      const int slot = k % kStagesC;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_full[slot], (k / kStagesC) & 1, abort, to));
+      if (!ok) {
+        if (lane == 0) conv_abort(abort, a.lc.err);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a_lo = lo0 + static_cast<uint32_t>(slot * (kStageC >> 4));
+      const uint32_t b_lo = a_lo + static_cast<uint32_t>(kATile >> 4);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)  // 16 channels (32 bytes) per MMA
+        umma_ss_elect_lo(tmem, a_lo + kk * 2, b_lo + kk * 2, hi, idesc, (k > 0 || kk > 0) ? 1u : 0u);
+      umma_commit_elect(&bar_empty[slot]);
+    }
+    // Also on the failure path: every issued MMA completes before TMEM is freed.
+    umma_commit_elect(&bar_acc);
+    mbar_wait(&bar_acc, 0, nullptr, to);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lanes 32q .. 32q+31
+    const int r = q * 32 + lane;
+    const int h = h0 + r / kPatchW, w = w0 + r % kPatchW;
+    const bool done = __all_sync(0xffffffffu, mbar_wait(&bar_acc, 0, abort, to));
+    if (!done && lane == 0) conv_abort(abort, a.lc.err);
+    if (done && !*abort) {
+      tc_fence_after();
+      const bool inside = h < a.H && w < a.W;
+      __nv_bfloat16* dst =
+          a.y + ((((size_t)b * a.T + t) * a.H + h) * a.W + w) * (size_t)a.c_out + n0;
+      for (int c = 0; c < a.n_tile / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c * 32), v);
+        tmem_ld_wait_regs(v);
+        if (inside) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float lo = __uint_as_float(v[2 * i]), hi2 = __uint_as_float(v[2 * i + 1]);
+            if (a.bias) {
+              lo += a.bias[n0 + c * 32 + 2 * i];
+              hi2 += a.bias[n0 + c * 32 + 2 * i + 1];
+            }
+            pk[i] = pack_bf16x2(lo, hi2);
+          }
+          uint4* o = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kConvTmemCols);
+  }
+}
+
+// bf16 channels-last activations [B, frames, H, W, C] -> 5D tiled map, box
+// {64 c, 16 w, 8 h, 1, 1}, 128-byte swizzle, zero fill outside.
+bool make_tmap_act(CUtensorMap* map, const void* base, int B, int frames, int H, int W, int C) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t c2 = (cuuint64_t)C * 2;
+  cuuint64_t dims[5] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)frames, (cuuint64_t)B};
+  cuuint64_t strides[4] = {c2, c2 * W, c2 * W * H, c2 * W * H * frames};
+  cuuint32_t box[5] = {kChunkC, kPatchW, kPatchH, 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Weights [C_out, 27, C_in] -> 3D tiled map, box {64 c, 1 tap, n_tile rows}.
+bool make_tmap_wt(CUtensorMap* map, const void* base, int c_in, int c_out, int n_tile) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)c_in, 27, (cuuint64_t)c_out};
+  cuuint64_t strides[2] = {(cuuint64_t)c_in * 2, (cuuint64_t)c_in * 2 * 27};
+  cuuint32_t box[3] = {kChunkC, 1, (cuuint32_t)n_tile};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int conv3d_n_tile(int c_out) {
+  for (int n : {256, 192, 128, 64})
+    if (c_out % n == 0) return n;
+  return 0;
+}
+
+int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const float* bias, void* y, int B, int T,
+                         int H, int W, int c_in, int c_out, const LaunchCommon& lc, cudaStream_t s) {
+  const int n_tile = conv3d_n_tile(c_out);
+  if (n_tile == 0 || c_in % kChunkC != 0) return WAN_ERR_UNSUPPORTED;
+  ConvArgs a;
+  a.bias = bias;
+  a.y = static_cast<__nv_bfloat16*>(y);
+  a.B = B;
+  a.T = T;
+  a.H = H;
+  a.W = W;
+  a.c_in = c_in;
+  a.c_out = c_out;
+  a.n_tile = n_tile;
+  a.tiles_h = (H + kPatchH - 1) / kPatchH;
+  a.tiles_w = (W + kPatchW - 1) / kPatchW;
+  a.has_cache = cache != nullptr;
+  a.lc = lc;
+  const long long m_tiles = (long long)B * T * a.tiles_h * a.tiles_w;
+  if (m_tiles > INT_MAX || c_out / n_tile > 65535) return WAN_ERR_INVALID;
+
+  CUtensorMap tx, tc, tw;
+  if (!make_tmap_act(&tx, x, B, T, H, W, c_in) ||
+      !make_tmap_act(&tc, cache ? cache : x, B, cache ? 2 : T, H, W, c_in) ||
+      !make_tmap_wt(&tw, wt, c_in, c_out, n_tile))
+    return WAN_ERR_CUDA;
+  if (cudaFuncSetAttribute(causal_conv3d_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kConvSmem) !=
+      cudaSuccess)
+    return WAN_ERR_CUDA;
+  record_start(lc, s);
+  causal_conv3d_kernel<<<dim3(static_cast<unsigned>(m_tiles), c_out / n_tile), kConvThreads, kConvSmem, s>>>(tx, tc,
+                                                                                                          tw, a);
+  record_stop(lc, s);
+  return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+}
+
+}  // namespace wan

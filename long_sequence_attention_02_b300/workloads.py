@@ -62,3 +62,35 @@ WORKLOADS = {
     # profiler capture of the backward kernel.
     "train_32x32x32_fwd_bwd": Workload("train_32x32x32_fwd_bwd", "self_fwd_bwd", 1, (32, 32, 32), 12),
 }
+
+
+@dataclass(frozen=True)
+class ConvWorkload:
+    """One causal 3x3x3 Conv3d layer of the VAE on one chunk of frames
+    (channels last, bf16), with the previous chunk's cache.
+
+    The pages give the VAE's compression (4x in time, 8x8 in space, 16 latent
+    channels) and its chunking (chunks of up to 4 frames, a 2-frame cache) but
+    not its channel widths; the shapes below are decoder-scale layers of that
+    plan: 384 channels at 1/8 of a 720p frame and 192 at 1/2.
+    """
+    name: str
+    B: int
+    T: int
+    H: int
+    W: int
+    c_in: int
+    c_out: int
+    kind: str = "conv3d"
+
+    def flops(self) -> float:
+        """2 FLOP per multiply-add: 2 * outputs * C_out * 27 * C_in."""
+        return 2.0 * self.B * self.T * self.H * self.W * self.c_out * 27 * self.c_in
+
+
+CONV_WORKLOADS = {
+    # 4 frames of 90 x 160 (720p / 8), 384 -> 384: inputs fit L2; parity case
+    "wan_vae_conv3d_720p_384": ConvWorkload("wan_vae_conv3d_720p_384", 1, 4, 90, 160, 384, 384),
+    # 4 frames of 360 x 640 (720p / 2), 192 -> 192: 354 MB of input, > L2; the timed layer
+    "wan_vae_conv3d_360x640_192": ConvWorkload("wan_vae_conv3d_360x640_192", 1, 4, 360, 640, 192, 192),
+}

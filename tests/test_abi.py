@@ -189,3 +189,30 @@ def test_noalloc_rejects_problems_larger_than_its_scratch(lib):
     assert wan.wan_attn_fwd_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 1, g, 128, 128, FAKE, 0.088) == wan.WAN_ERR_INVALID
     assert wan.wan_attn_fwd_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 1, (0, 4, 4), 2, 128, FAKE, 0.088) == \
         wan.WAN_ERR_INVALID
+
+
+def test_conv3d_rejects_bad_arguments(lib):
+    # x [1, 4, 8, 16, 64], y [1, 4, 8, 16, 128], cache [1, 2, 8, 16, 64], weight [128, 27, 64]
+    frame = 8 * 16 * 64 * 2
+    X, Y, C, Wt = FAKE, FAKE + (1 << 24), FAKE + (2 << 24), FAKE + (3 << 24)
+    ok = dict(x=X, cache=C, weight=Wt, bias=FAKE + (4 << 24), y=Y, cache_out=C, B=1, T=4, H=8, W=16, c_in=64,
+              c_out=128, stream=0)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return wan.wan_vae_causal_conv3d(**a)
+
+    assert call(x=None) == wan.WAN_ERR_INVALID
+    assert call(weight=None) == wan.WAN_ERR_INVALID
+    assert call(y=None) == wan.WAN_ERR_INVALID
+    assert call(x=X + 8) == wan.WAN_ERR_INVALID
+    assert call(bias=FAKE + 2) == wan.WAN_ERR_INVALID
+    assert call(T=0) == wan.WAN_ERR_INVALID
+    assert call(H=-1) == wan.WAN_ERR_INVALID
+    assert call(c_in=96) == wan.WAN_ERR_UNSUPPORTED         # channels must be multiples of 64
+    assert call(c_out=32) == wan.WAN_ERR_UNSUPPORTED
+    assert call(y=X + frame) == wan.WAN_ERR_INVALID          # output overlapping the input
+    assert call(cache_out=X) == wan.WAN_ERR_INVALID          # next cache over the input
+    assert call(cache_out=C + 64) == wan.WAN_ERR_INVALID     # partly over the cache it reads
+    assert call(B=0, x=None, weight=None, y=None) == wan.WAN_OK

@@ -1,0 +1,106 @@
+"""Causal Conv3d of the Wan-VAE (with its feature cache) on the GPU, through
+the C ABI, against the fp64 oracle.
+
+Inputs are seeded N(0, 1) bf16; weights are N(0, 1) bf16 scaled by a power of
+two near 1/sqrt(27 * C_in) (exact in bf16), so outputs are O(1) and the
+workload tolerances (max-abs 2e-2, relative L2 5e-3) apply: the only
+rounding beyond fp32 accumulation is the bf16 output (relative 2^-9).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import long_sequence_attention_02_b300 as wan
+from long_sequence_attention_02_b300 import synth
+from oracle import vae
+from tests._util import bf16_round, bits, compare, dev_to_f64, f64, to_dev
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+def _layer(seed, B, T, H, W, c_in, c_out, with_cache, with_bias):
+    x = bits(seed, synth.STREAM_Q, (B, T, H, W, c_in))
+    cache = bits(seed, synth.STREAM_K, (B, 2, H, W, c_in)) if with_cache else None
+    shift = round(math.log2(math.sqrt(27 * c_in)))
+    wt = bf16_round(f64(bits(seed, synth.STREAM_V, (c_out, 3, 3, 3, c_in))) * 2.0 ** -shift)
+    bias = (f64(bits(seed, synth.STREAM_DO, (c_out,))) * 0.25).astype(np.float32) if with_bias else None
+    return x, cache, wt, bias
+
+
+def _run(x, cache, wt, bias, cache_out=True, stream=None):
+    B, T, H, W, c_in = x.shape
+    c_out = wt.shape[0]
+    y = torch.empty(B, T, H, W, c_out, dtype=torch.bfloat16, device="cuda")
+    co = torch.empty(B, 2, H, W, c_in, dtype=torch.bfloat16, device="cuda") if cache_out else None
+    xd = x if isinstance(x, torch.Tensor) else to_dev(x)
+    cd = None if cache is None else (cache if isinstance(cache, torch.Tensor) else to_dev(cache))
+    bd = None if bias is None else torch.from_numpy(bias).cuda()
+    wan.check(wan.wan_vae_causal_conv3d(xd, cd, to_dev(wt), bd, y, co, B, T, H, W, c_in, c_out, stream), "conv3d")
+    wan.check(wan.wan_get_device_status())
+    return y, co
+
+
+@pytest.mark.parametrize("B,T,H,W,c_in,c_out,with_cache,with_bias", [
+    (2, 3, 10, 19, 64, 128, True, True),     # ragged 8 x 16 patches, N = 128
+    (1, 1, 8, 16, 128, 192, False, True),    # first chunk of one frame, N = 192
+    (1, 2, 5, 33, 64, 256, True, False),     # N = 256, no bias
+    (1, 4, 9, 17, 128, 320, False, True),    # N = 64 (320 = 5 x 64)
+])
+def test_conv3d_every_output(B, T, H, W, c_in, c_out, with_cache, with_bias):
+    x, cache, wt, bias = _layer(21, B, T, H, W, c_in, c_out, with_cache, with_bias)
+    y, co = _run(x, cache, wt, bias)
+    y_ref, cache_ref = vae.causal_conv3d(f64(x), f64(wt), None if bias is None else bias.astype(np.float64),
+                                         None if cache is None else f64(cache))
+    compare(dev_to_f64(y), y_ref, "y")
+    assert np.array_equal(dev_to_f64(co), cache_ref), "next cache"
+
+
+def test_conv3d_chunks_through_the_cache_equal_the_whole_video():
+    """Nine frames in chunks of 1, 4 and 4, each chunk fed the cache the
+    previous call returned: equal to the oracle's whole-sequence layer, and
+    bit for bit equal to the GPU's own whole-sequence call."""
+    B, T, H, W, c_in, c_out = 1, 9, 8, 20, 64, 128
+    x, _, wt, bias = _layer(22, B, T, H, W, c_in, c_out, False, True)
+    xd = to_dev(x)
+    whole, _ = _run(xd, None, wt, bias)
+    outs, cache, t0 = [], None, 0
+    for n in (1, 4, 4):
+        y, cache = _run(xd[:, t0:t0 + n].contiguous(), cache, wt, bias)
+        outs.append(y)
+        t0 += n
+    chunked = torch.cat(outs, dim=1)
+    assert torch.equal(chunked, whole)
+    y_ref, _ = vae.causal_conv3d(f64(x), f64(wt), bias.astype(np.float64))
+    compare(dev_to_f64(chunked), y_ref, "chunked y")
+
+
+def test_conv3d_without_cache_output_on_a_side_stream():
+    x, cache, wt, bias = _layer(23, 1, 2, 8, 16, 64, 64, True, True)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y, co = _run(x, cache, wt, bias, cache_out=False, stream=s)
+    s.synchronize()
+    assert co is None
+    y_ref, _ = vae.causal_conv3d(f64(x), f64(wt), bias.astype(np.float64), f64(cache))
+    compare(dev_to_f64(y), y_ref, "y (side stream)")
+
+
+def test_conv3d_full_size_sampled():
+    """The 720p decoder-scale layer (4 frames of 90 x 160, 384 -> 384 channels,
+    with a cache) on 512 seeded sampled output positions."""
+    from long_sequence_attention_02_b300.workloads import CONV_WORKLOADS
+
+    w = CONV_WORKLOADS["wan_vae_conv3d_720p_384"]
+    x, cache, wt, bias = _layer(24, w.B, w.T, w.H, w.W, w.c_in, w.c_out, True, True)
+    y, co = _run(x, cache, wt, bias)
+    rng = np.random.default_rng(25)
+    n = 512
+    pos = list(zip(rng.integers(0, w.B, n), rng.integers(0, w.T, n), rng.integers(0, w.H, n),
+                   rng.integers(0, w.W, n)))
+    pos[:4] = [(0, 0, 0, 0), (0, w.T - 1, w.H - 1, w.W - 1), (0, 0, w.H - 1, 0), (0, 1, 0, w.W - 1)]
+    got = dev_to_f64(torch.stack([y[p] for p in pos]))
+    ref = vae.causal_conv3d_at(f64(x), f64(wt), bias.astype(np.float64), f64(cache), pos)
+    compare(got, ref, "y (sampled)")
+    assert np.array_equal(dev_to_f64(co), f64(x[:, -2:])), "next cache"

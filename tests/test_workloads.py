@@ -42,3 +42,14 @@ def test_bad_video_shapes():
         workloads.latent_grid(80, 480, 832)
     with pytest.raises(ValueError):
         workloads.latent_grid(81, 480, 830)
+
+
+def test_conv_workloads():
+    from oracle import vae
+
+    for w in workloads.CONV_WORKLOADS.values():
+        assert w.kind == "conv3d" and w.c_in % 64 == 0 and w.c_out % 64 == 0
+        assert w.T <= 4                      # chunks of at most four frames
+        assert w.flops() == vae.conv3d_flops(w.B, w.T, w.H, w.W, w.c_in, w.c_out)
+    big = workloads.CONV_WORKLOADS["wan_vae_conv3d_360x640_192"]
+    assert big.B * big.T * big.H * big.W * big.c_in * 2 > 126 * 2**20   # the timed layer's input exceeds L2
