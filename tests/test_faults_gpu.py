@@ -75,3 +75,20 @@ def test_timeout_in_backward():
     dq_r, dk_r, dv_r = ref.self_attention_bwd(f64(qb), f64(kb), f64(vb), f64(dob), grid)
     compare(dev_to_f64(dq), dq_r, "dQ after recovery")
     compare(dev_to_f64(dv), dv_r, "dV after recovery")
+
+
+def test_timeout_in_fp8_forward():
+    grid, (qb, kb, vb) = _tiny()
+    q, k, v = to_dev(qb), to_dev(kb), to_dev(vb)
+    wan.check(wan.wan_debug_inject_stall(1, 100))
+    try:
+        wan.attention_forward_fp8(q, k, v, grid)
+    finally:
+        wan.wan_debug_inject_stall(0, 100)
+    assert wan.wan_get_device_status() == wan.WAN_ERR_TIMEOUT
+    o, lse = wan.attention_forward_fp8(q, k, v, grid)
+    assert wan.wan_get_device_status() == wan.WAN_OK
+    o_ref, lse_ref = ref.self_attention_fwd(f64(qb), f64(kb), f64(vb), grid)
+    # the FP8 tolerance (derived in test_fp8_gpu.py): relative L2 0.12 on O, LSE max-abs 0.2
+    compare(dev_to_f64(o), o_ref, "fp8 O after recovery", max_abs=0.15 * float(np.abs(o_ref).max()), rel_l2=0.12)
+    compare(dev_to_f64(lse), lse_ref, "fp8 LSE after recovery", max_abs=0.2, rel_l2=float("inf"))
