@@ -31,6 +31,22 @@ def test_reference_arm_prints_one_json_line():
     assert rec["config"]["workload"] == "tiny_3x8x8_h2"
 
 
+def test_conv_reference_arm_and_cpu_baseline():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          "wan_vae_conv3d_360x640_192", "--steps", "1", "--warmup", "1", "--ref-rows", "8"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["metric"] == bench.CONV_METRIC and rec["value"] > 0
+    assert rec["config"]["kind"] == "conv3d" and rec["config"]["c_out"] == 192
+    from long_sequence_attention_02_b300.workloads import CONV_WORKLOADS
+
+    cb = bench.cpu_baseline(CONV_WORKLOADS["wan_vae_conv3d_720p_384"], 16)
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and "output positions" in cb["sample"]
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
