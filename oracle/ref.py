@@ -305,6 +305,53 @@ def self_attention_bwd_dq_rows(q_rows, do_rows, rows, k_head, v_head, grid,
     return rope_rotate(dqr, ang[rows], inverse=True)
 
 
+def self_attention_bwd_dkdv_rows(q_head, k_head, v_head, do_head, key_rows, grid, theta=DEFAULT_THETA,
+                                 scale=None, block=64, row_map=map):
+    """dK and dV of selected key rows of ONE (b, h).
+
+    q_head, k_head, v_head, do_head: float64 [L, d] of the head (pre-RoPE);
+    key_rows: the token indices J of the key rows wanted. Every query row
+    contributes to a key row's gradient, so all L query rows are visited:
+      1. the forward over all keys gives LSE_i and O_i of every query row,
+         and D_i = dO_i . O_i;
+      2. for the selected keys only, with P_ij = exp(scale qr_i . kr_j - LSE_i)
+         (the softmax entries of column j), dP_ij = dO_i . v_j and
+         dS_ij = P_ij (dP_ij - D_i):
+           dKr_j = scale sum_i dS_ij qr_i,   dV_j = sum_i P_ij dO_i,
+           dK_j = R(pos_j)^T dKr_j.
+    These are the columns J of the full backward (self_attention_bwd).
+    `row_map` maps the forward over blocks of query rows; the builtin map by
+    default (a thread pool's map gives the same result, faster).
+    Returns dK [|J|, d] and dV [|J|, d].
+    """
+    L, d = k_head.shape
+    F, Hp, Wp = grid
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    ang = rope_angles(F, Hp, Wp, d, theta)
+    key_rows = np.asarray(key_rows)
+    qr = rope_rotate(q_head, ang)
+    kr = rope_rotate(k_head, ang)
+
+    def forward_block(bounds):
+        i0, i1 = bounds
+        return softmax_attention(qr[i0:i1], kr, v_head, scale)
+
+    parts = list(row_map(forward_block, list(_row_blocks(L, block))))
+    o = np.concatenate([p[0] for p in parts])
+    lse = np.concatenate([p[1] for p in parts])
+    d_i = np.sum(do_head * o, axis=1)
+    kr_j, v_j = kr[key_rows], v_head[key_rows]
+    dkr = np.zeros((len(key_rows), d))
+    dv = np.zeros((len(key_rows), d))
+    for i0, i1 in _row_blocks(L, 4096):
+        p = np.exp(scale * (qr[i0:i1] @ kr_j.T) - lse[i0:i1, None])
+        dp = do_head[i0:i1] @ v_j.T
+        ds = p * (dp - d_i[i0:i1, None])
+        dkr += scale * (ds.T @ qr[i0:i1])
+        dv += p.T @ do_head[i0:i1]
+    return rope_rotate(dkr, ang[key_rows], inverse=True), dv
+
+
 # ---------------------------------------------------------------------------
 # Partial results over disjoint key sets (the state a ring step carries)
 

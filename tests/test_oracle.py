@@ -289,6 +289,49 @@ def test_row_subset_helpers_match_full():
     np.testing.assert_allclose(dq_r, dq[0, rows, 0], atol=1e-13)
 
 
+def test_key_row_gradients_match_full_backward():
+    """dK / dV of selected key rows (all query rows visited, LSE and D from
+    the oracle's own forward) equal those rows of the full backward, whether
+    the forward blocks run in order or through a thread pool, and with a
+    block that does not divide L."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    grid = (3, 5, 7)
+    L, d = 105, 128
+    q, k, v, do = (_rand(1, L, 1, d) for _ in range(4))
+    _, dk, dv = ref.self_attention_bwd(q, k, v, do, grid)
+    keys = np.array([0, 104, 51, 7, 52])
+    args = (q[0, :, 0], k[0, :, 0], v[0, :, 0], do[0, :, 0], keys, grid)
+    dk_r, dv_r = ref.self_attention_bwd_dkdv_rows(*args, block=16)
+    np.testing.assert_allclose(dk_r, dk[0, keys, 0], atol=1e-12)
+    np.testing.assert_allclose(dv_r, dv[0, keys, 0], atol=1e-12)
+    with ThreadPoolExecutor(4) as ex:
+        dk_t, dv_t = ref.self_attention_bwd_dkdv_rows(*args, block=10, row_map=ex.map)
+    np.testing.assert_allclose(dk_t, dk_r, atol=1e-13)
+    np.testing.assert_allclose(dv_t, dv_r, atol=1e-13)
+
+
+def test_key_row_gradients_central_differences():
+    """The key-row helper against central differences of sum(O * dO) taken
+    directly (not through the full backward)."""
+    grid = (2, 2, 3)
+    L, d = 12, 128
+    theta, scale = 10000.0, 1.0 / math.sqrt(d)
+    q, k, v, do = (_rand(1, L, 1, d) for _ in range(4))
+    keys = np.array([3, 11])
+    dk_r, dv_r = ref.self_attention_bwd_dkdv_rows(q[0, :, 0], k[0, :, 0], v[0, :, 0], do[0, :, 0], keys, grid)
+    eps = 1e-5
+    for name, g in (("k", dk_r), ("v", dv_r)):
+        for a, j in enumerate(keys):
+            for x in (0, 45, 90, 127):
+                plus, minus = {"k": k.copy(), "v": v.copy()}, {"k": k.copy(), "v": v.copy()}
+                plus[name][0, j, 0, x] += eps
+                minus[name][0, j, 0, x] -= eps
+                fd = (_objective(q, plus["k"], plus["v"], do, grid, theta, scale)
+                      - _objective(q, minus["k"], minus["v"], do, grid, theta, scale)) / (2 * eps)
+                assert abs(fd - g[a, x]) < 1e-7 * max(1.0, abs(g[a, x])), (name, j, x, fd, g[a, x])
+
+
 # ---------------------------------------------------------------------------
 # Backward
 
