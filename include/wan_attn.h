@@ -216,10 +216,25 @@ int wan_get_device_status(void* stream);
 int wan_profile_set_events(void* start, void* stop);
 
 /*
- * Test hook (not for production use): make the next `count` attention kernel
- * launches on this device skip one producer arrival so that their consumers'
- * bounded waits expire after `timeout_ms`, exercising the timeout path without
- * faulting. count = 0 restores normal operation.
+ * The same hook for one pass of an entry point: WAN_PASS_MAIN (the main
+ * kernel, as wan_profile_set_events), WAN_PASS_ROPE (the K rotation
+ * pre-pass of wan_attn_fwd, wan_attn_fwd_ring_step and wan_attn_bwd),
+ * WAN_PASS_ROWS (the row pass of wan_attn_bwd: D = rowsum(dO * O) and
+ * LSE * log2 e) or WAN_PASS_POST (the dQ post-pass of wan_attn_bwd:
+ * R^T dQ_acc -> bf16). Events set for several passes are all consumed, and
+ * cleared, by the next entry-point call; a pass that call does not run
+ * leaves its events unrecorded. WAN_ERR_INVALID for an unknown pass or
+ * exactly one NULL event.
+ */
+enum { WAN_PASS_MAIN = 0, WAN_PASS_ROPE = 1, WAN_PASS_ROWS = 2, WAN_PASS_POST = 3 };
+int wan_profile_set_pass_events(int pass, void* start, void* stop);
+
+/*
+ * Test hook (not for production use): make the next `count` main-kernel
+ * launches (attention forward, cross-attention, backward, FP8 forward or VAE
+ * Conv3d) skip one producer arrival so that their consumers' bounded waits
+ * expire after `timeout_ms`, exercising the timeout path without faulting.
+ * count = 0 restores normal operation.
  */
 int wan_debug_inject_stall(int count, int timeout_ms);
 

@@ -35,7 +35,12 @@ EXPORTED = (
     "wan_attn_workspace_size", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
     "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall", "wan_attn_fwd_noalloc",
     "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual", "wan_attn_fwd_fp8", "wan_vae_causal_conv3d",
+    "wan_profile_set_pass_events",
 )
+WAN_PASS_MAIN = 0
+WAN_PASS_ROPE = 1
+WAN_PASS_ROWS = 2
+WAN_PASS_POST = 3
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 NOALLOC_MAX_ROW_HEADS = NOALLOC_SCRATCH_BYTES // 256
 
@@ -82,10 +87,11 @@ def load_library(path: str = LIB_PATH):
     lib.wan_get_device_status.argtypes = [vp]
     lib.wan_debug_inject_stall.argtypes = [i32, i32]
     lib.wan_profile_set_events.argtypes = [vp, vp]
+    lib.wan_profile_set_pass_events.argtypes = [i32, vp, vp]
     for name in ("wan_rope3d_tables", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
                  "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall",
                  "wan_attn_fwd_noalloc", "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual", "wan_attn_fwd_fp8",
-                 "wan_vae_causal_conv3d"):
+                 "wan_vae_causal_conv3d", "wan_profile_set_pass_events"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -208,6 +214,15 @@ def wan_profile_set_events(start, stop) -> int:
     if any(h == 0 for h in handles):
         raise ValueError("wan_profile_set_events: event has no CUDA handle yet (record it once first)")
     return load_library().wan_profile_set_events(*handles)
+
+
+def wan_profile_set_pass_events(pass_, start, stop) -> int:
+    """Events around one pass (WAN_PASS_*) of the next entry-point call; same
+    event rules as wan_profile_set_events."""
+    handles = [None if e is None else e.cuda_event for e in (start, stop)]
+    if any(h == 0 for h in handles):
+        raise ValueError("wan_profile_set_pass_events: event has no CUDA handle yet (record it once first)")
+    return load_library().wan_profile_set_pass_events(int(pass_), *handles)
 
 
 def wan_debug_inject_stall(count: int, timeout_ms: int) -> int:

@@ -29,8 +29,7 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 int g_stall_launches = 0;
 uint64_t g_stall_timeout_ns = 0;
-cudaEvent_t g_prof_start = nullptr;
-cudaEvent_t g_prof_stop = nullptr;
+cudaEvent_t g_prof[wan::kNumPasses][2] = {};  // profiling hook, one-shot (guarded by g_mu)
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -80,9 +79,11 @@ wan::LaunchCommon launch_common(const DeviceState& st) {
   lc.timeout_ns = kDefaultTimeoutNs;
   lc.stall = 0;
   std::lock_guard<std::mutex> lk(g_mu);
-  lc.ev_start = g_prof_start;
-  lc.ev_stop = g_prof_stop;
-  g_prof_start = g_prof_stop = nullptr;
+  for (int p = 0; p < wan::kNumPasses; ++p)
+    for (int i = 0; i < 2; ++i) {
+      lc.ev[p][i] = g_prof[p][i];
+      g_prof[p][i] = nullptr;
+    }
   if (g_stall_launches > 0) {
     --g_stall_launches;
     lc.stall = 1;
@@ -201,9 +202,11 @@ int wan_attn_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   if ((rc = device_state(&st)) != WAN_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const wan::RopeTables tab = split_tables(tables, g);
+  const wan::LaunchCommon lc = launch_common(*st);
+  wan::record_pass(lc, wan::kPassRope, 0, s);
   if (wan::launch_rope_rotate_bf16(k, workspace, B, g, H, tab, false, s) != cudaSuccess) return WAN_ERR_CUDA;
-  return wan::launch_attn_fwd(q, workspace, v, o, lse, B, (int)L, (int)L, H, g, tab, true, nullptr, scale,
-                              launch_common(*st), s);
+  wan::record_pass(lc, wan::kPassRope, 1, s);
+  return wan::launch_attn_fwd(q, workspace, v, o, lse, B, (int)L, (int)L, H, g, tab, true, nullptr, scale, lc, s);
 }
 
 int wan_xattn_fwd(const void* q, const void* k, const void* v, const int32_t* kv_lens, int Lk, void* o,
@@ -289,10 +292,13 @@ int wan_attn_fwd_ring_step(const void* q, const void* k, const void* v, void* o,
   if ((rc = device_state(&st)) != WAN_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const wan::RopeTables tab = split_tables(tables, g);
+  const wan::LaunchCommon lc = launch_common(*st);
+  wan::record_pass(lc, wan::kPassRope, 0, s);
   if (wan::launch_rope_rotate_bf16_rows(k, workspace, B, kv_len, kv_start, g, H, tab, false, s) != cudaSuccess)
     return WAN_ERR_CUDA;
-  return wan::launch_attn_fwd(q, workspace, v, o, lse, B, q_len, kv_len, H, g, tab, true, nullptr, scale,
-                              launch_common(*st), s, q_start, accumulate ? wan::kMergeLse : wan::kMergeNone);
+  wan::record_pass(lc, wan::kPassRope, 1, s);
+  return wan::launch_attn_fwd(q, workspace, v, o, lse, B, q_len, kv_len, H, g, tab, true, nullptr, scale, lc, s,
+                              q_start, accumulate ? wan::kMergeLse : wan::kMergeNone);
 }
 
 int wan_xattn_fwd_dual(const void* q, const void* k_txt, const void* v_txt, const int32_t* lens_txt, int Lk_txt,
@@ -333,13 +339,15 @@ int wan_get_device_status(void* stream) {
   return v == 0 ? WAN_OK : v;
 }
 
-int wan_profile_set_events(void* start, void* stop) {
-  if ((start == nullptr) != (stop == nullptr)) return WAN_ERR_INVALID;
+int wan_profile_set_pass_events(int pass, void* start, void* stop) {
+  if (pass < 0 || pass >= wan::kNumPasses || (start == nullptr) != (stop == nullptr)) return WAN_ERR_INVALID;
   std::lock_guard<std::mutex> lk(g_mu);
-  g_prof_start = static_cast<cudaEvent_t>(start);
-  g_prof_stop = static_cast<cudaEvent_t>(stop);
+  g_prof[pass][0] = static_cast<cudaEvent_t>(start);
+  g_prof[pass][1] = static_cast<cudaEvent_t>(stop);
   return WAN_OK;
 }
+
+int wan_profile_set_events(void* start, void* stop) { return wan_profile_set_pass_events(WAN_PASS_MAIN, start, stop); }
 
 int wan_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g,
                          int H, int head_dim, const float* tables, float scale, void* stream) {

@@ -126,13 +126,15 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint32_t tx = static_cast<uint32_t>(kATile + a.n_tile * 128);
-      int issued = 0;
+      int k_end = 0;  // K steps walked (issued, or withheld by the test hook)
       for (int k = 0; k < k_steps; ++k) {
         const int slot = k % kStagesC;
         if (k >= kStagesC && !mbar_wait(&bar_empty[slot], ((k / kStagesC) - 1) & 1, abort, to)) {
           conv_abort(abort, a.lc.err);
           break;
         }
+        k_end = k + 1;
+        if (a.lc.stall && k == 1) continue;  // test hook: K step 1 never arrives
         const int tap = k / c_steps;
         const int c0 = (k % c_steps) * kChunkC;
         const int kt = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
@@ -144,10 +146,11 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         else  // before a first chunk (ti < 0) the box lies outside x and reads zeros
           tma_load_5d(sa, &tm_x, &bar_full[slot], c0, w0 + kw - 1, h0 + kh - 1, ti, b);
         tma_load_3d(sa + kATile, &tm_w, &bar_full[slot], c0, tap, n0);
-        ++issued;
       }
-      // Every copy this warp issued lands before the CTA may exit.
-      for (int k = issued - kStagesC < 0 ? 0 : issued - kStagesC; k < issued; ++k)
+      // Every copy this warp issued lands before the CTA may exit (the last
+      // fill of each slot is that barrier's latest phase; a withheld step's
+      // wait just runs out).
+      for (int k = k_end - kStagesC < 0 ? 0 : k_end - kStagesC; k < k_end; ++k)
         mbar_wait(&bar_full[k % kStagesC], (k / kStagesC) & 1, nullptr, to);
     }
     __syncwarp();

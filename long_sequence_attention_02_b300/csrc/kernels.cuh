@@ -20,20 +20,28 @@ struct RopeTables {
   const float2* w;  // [Wp][kPairsW]
 };
 
+// Passes of an entry point that the profiling hook can bracket with events
+// (the values of the WAN_PASS_* constants of the C ABI).
+enum ProfPass : int {
+  kPassMain = 0,  // the main kernel (attention, backward, FP8 attention, Conv3d)
+  kPassRope = 1,  // the K rotation pre-pass (forward, Ring step, backward)
+  kPassRows = 2,  // the backward's row pass (D and LSE * log2 e)
+  kPassPost = 3,  // the backward's dQ post-pass (R^T dQ_acc -> bf16)
+  kNumPasses = 4,
+};
+
 struct LaunchCommon {
   int* err;             // device error word
   uint64_t timeout_ns;  // bound of every device-side wait
   int stall;            // test hook: producer withholds one tile
-  cudaEvent_t ev_start; // profiling hook: recorded around the main kernel (may be null)
-  cudaEvent_t ev_stop;
+  cudaEvent_t ev[kNumPasses][2];  // profiling hook: {start, stop} around each pass (may be null)
 };
 
-inline void record_start(const LaunchCommon& lc, cudaStream_t s) {
-  if (lc.ev_start) cudaEventRecord(lc.ev_start, s);
+inline void record_pass(const LaunchCommon& lc, int pass, int which, cudaStream_t s) {
+  if (lc.ev[pass][which]) cudaEventRecord(lc.ev[pass][which], s);
 }
-inline void record_stop(const LaunchCommon& lc, cudaStream_t s) {
-  if (lc.ev_stop) cudaEventRecord(lc.ev_stop, s);
-}
+inline void record_start(const LaunchCommon& lc, cudaStream_t s) { record_pass(lc, kPassMain, 0, s); }
+inline void record_stop(const LaunchCommon& lc, cudaStream_t s) { record_pass(lc, kPassMain, 1, s); }
 
 // y = R(pos) x (or R(pos)^T x when inverse) for bf16 [B, L, H, 128]; y may equal x.
 cudaError_t launch_rope_rotate_bf16(const void* x, void* y, int B, wan_grid_t g, int H, RopeTables tab,

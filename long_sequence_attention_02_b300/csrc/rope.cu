@@ -5,9 +5,9 @@
 // turn by the band's angle for the token's coordinate on that axis; the
 // angles come from the caller's fp32 {cos, sin} tables.
 //
-// One thread handles one 16-byte chunk (8 elements = 4 rotary pairs); a warp
-// covers 512 contiguous bytes, so loads and stores are fully coalesced. The
-// grid is a multiple of the SM count and strides over the tensor.
+// Loads and stores are 16-byte chunks (8 elements = 4 rotary pairs); the
+// threads of a block cover contiguous bytes, so they are fully coalesced.
+// The grids are multiples of the SM count and stride over the tensor.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -21,71 +21,118 @@ __device__ __forceinline__ float2 rope_cs(const RopeTables& tab, int pair, int t
 
 // x holds L consecutive tokens per batch item, the first one being token
 // pos0 of the grid (pos0 > 0 for a chunk of a longer sequence).
+//
+// A block of 128 threads rotates one token (all H heads) per step of a
+// grid-stride loop over tokens. Thread (c, g) = (tid % 16, tid / 16) owns the
+// 16-byte chunk c of heads g, g + 8, g + 16, ...: the angles of a chunk (its
+// four rotary pairs) depend only on the token, so each thread decodes the
+// token's grid coordinates and reads its four {cos, sin} pairs once per token
+// and reuses them for every head it rotates. A block's loads of one token
+// cover H * 256 contiguous bytes; up to kHeadsPerPass of a thread's heads are
+// loaded before the first is used.
 template <bool kInverse>
-__global__ void __launch_bounds__(256) rope_rotate_kernel(const uint4* x, uint4* y,
-                                                          long long n_chunks, int H, int Hp, int Wp, int L,
-                                                          int pos0, RopeTables tab) {
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_chunks; i += stride) {
-    const int c = (int)(i & 15);          // chunk within the 128-wide head
-    const long long rowhead = i >> 4;     // (b*L + l)*H + h
-    const long long bl = rowhead / H;     // b*L + l
-    const int l = (int)(bl % L) + pos0;
+__global__ void __launch_bounds__(128) rope_rotate_kernel(const uint4* x, uint4* y, long long n_tokens, int H,
+                                                          int Hp, int Wp, int L, int pos0, RopeTables tab) {
+  constexpr int kHeadsPerPass = 8;
+  const int c = threadIdx.x & 15;
+  const int g = threadIdx.x >> 4;
+  int band[4], j[4], row[4];
+  const float2* base[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int pair = c * 4 + k;
+    band[k] = pair < kPairsT ? 0 : (pair < kPairsT + kPairsH ? 1 : 2);
+    j[k] = band[k] == 0 ? pair : (band[k] == 1 ? pair - kPairsT : pair - kPairsT - kPairsH);
+    row[k] = band[k] == 0 ? kPairsT : (band[k] == 1 ? kPairsH : kPairsW);
+    base[k] = band[k] == 0 ? tab.t : (band[k] == 1 ? tab.h : tab.w);
+  }
+  for (long long tok = blockIdx.x; tok < n_tokens; tok += gridDim.x) {
+    const int l = static_cast<int>(tok % L) + pos0;
     const int w = l % Wp;
     const int hh = (l / Wp) % Hp;
     const int t = l / (Wp * Hp);
-    uint4 v = x[i];
-    uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+    float2 cs[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float2 cs = rope_cs(tab, c * 4 + k, t, hh, w);
-      const float sn = kInverse ? -cs.y : cs.y;
-      const float a = __uint_as_float(wd[k] << 16);
-      const float b = __uint_as_float(wd[k] & 0xFFFF0000u);
-      wd[k] = pack_bf16x2(a * cs.x - b * sn, a * sn + b * cs.x);
+      const int pos = band[k] == 0 ? t : (band[k] == 1 ? hh : w);
+      cs[k] = base[k][pos * row[k] + j[k]];
+      if (kInverse) cs[k].y = -cs[k].y;
     }
-    y[i] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    const size_t tok_chunk = static_cast<size_t>(tok) * H * 16 + c;
+    for (int h0 = g; h0 < H; h0 += 8 * kHeadsPerPass) {
+      uint4 v[kHeadsPerPass];
+#pragma unroll
+      for (int u = 0; u < kHeadsPerPass; ++u)
+        if (h0 + 8 * u < H) v[u] = x[tok_chunk + static_cast<size_t>(h0 + 8 * u) * 16];
+#pragma unroll
+      for (int u = 0; u < kHeadsPerPass; ++u) {
+        if (h0 + 8 * u >= H) break;
+        uint32_t wd[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float a = __uint_as_float(wd[k] << 16);
+          const float b = __uint_as_float(wd[k] & 0xFFFF0000u);
+          wd[k] = pack_bf16x2(a * cs[k].x - b * cs[k].y, a * cs[k].y + b * cs[k].x);
+        }
+        y[tok_chunk + static_cast<size_t>(h0 + 8 * u) * 16] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      }
+    }
   }
 }
 
-// dQ path of the backward: fp32 [B, L, H, 128] -> R(pos)^T x -> bf16.
-// One thread per 8 elements (two 16-byte fp32 loads, one 16-byte bf16 store).
-__global__ void __launch_bounds__(256) rope_unrotate_f32_kernel(const float4* x, uint4* y, long long n_chunks, int H,
+// dQ path of the backward: fp32 [B, L, H, 128] -> R(pos)^T x -> bf16, with
+// the same token-per-block walk as rope_rotate_kernel: thread (c, g) reads the
+// 32-byte fp32 chunk c (8 elements) of heads g, g + 8, ... and writes 16 bytes.
+__global__ void __launch_bounds__(128) rope_unrotate_f32_kernel(const float4* x, uint4* y, long long n_tokens, int H,
                                                                 int Hp, int Wp, int L, RopeTables tab) {
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_chunks; i += stride) {
-    const int c = (int)(i & 15);
-    const long long bl = (i >> 4) / H;
-    const int l = (int)(bl % L);
+  constexpr int kHeadsPerPass = 4;
+  const int c = threadIdx.x & 15;
+  const int g = threadIdx.x >> 4;
+  for (long long tok = blockIdx.x; tok < n_tokens; tok += gridDim.x) {
+    const int l = static_cast<int>(tok % L);
     const int w = l % Wp;
     const int hh = (l / Wp) % Hp;
     const int t = l / (Wp * Hp);
-    const float4 u0 = x[2 * i];
-    const float4 u1 = x[2 * i + 1];
-    const float v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-    uint32_t wd[4];
+    float2 cs[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 cs = rope_cs(tab, c * 4 + k, t, hh, w);
-      const float a = v[2 * k], b = v[2 * k + 1];
-      wd[k] = pack_bf16x2(a * cs.x + b * cs.y, b * cs.x - a * cs.y);
+    for (int k = 0; k < 4; ++k) cs[k] = rope_cs(tab, c * 4 + k, t, hh, w);
+    const size_t tok_chunk = static_cast<size_t>(tok) * H * 16 + c;
+    for (int h0 = g; h0 < H; h0 += 8 * kHeadsPerPass) {
+      float4 u0[kHeadsPerPass], u1[kHeadsPerPass];
+#pragma unroll
+      for (int u = 0; u < kHeadsPerPass; ++u)
+        if (h0 + 8 * u < H) {
+          const size_t i = tok_chunk + static_cast<size_t>(h0 + 8 * u) * 16;
+          u0[u] = x[2 * i];
+          u1[u] = x[2 * i + 1];
+        }
+#pragma unroll
+      for (int u = 0; u < kHeadsPerPass; ++u) {
+        if (h0 + 8 * u >= H) break;
+        const float v[8] = {u0[u].x, u0[u].y, u0[u].z, u0[u].w, u1[u].x, u1[u].y, u1[u].z, u1[u].w};
+        uint32_t wd[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float a = v[2 * k], b = v[2 * k + 1];
+          wd[k] = pack_bf16x2(a * cs[k].x + b * cs[k].y, b * cs[k].x - a * cs[k].y);
+        }
+        y[tok_chunk + static_cast<size_t>(h0 + 8 * u) * 16] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      }
     }
-    y[i] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
   }
 }
 
 cudaError_t launch_rope_unrotate_f32(const float* x, void* y, int B, wan_grid_t g, int H, RopeTables tab,
                                      cudaStream_t s) {
   const int L = g.F * g.Hp * g.Wp;
-  const long long n_chunks = (long long)B * L * H * (kHeadDim / 8);
-  if (n_chunks == 0) return cudaSuccess;
+  const long long n_tokens = (long long)B * L;
+  if (n_tokens == 0 || H == 0) return cudaSuccess;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  long long want = (n_chunks + 255) / 256;
-  long long cap = (long long)sms * 8;
-  const int blocks = (int)(want < cap ? want : cap);
-  rope_unrotate_f32_kernel<<<blocks, 256, 0, s>>>((const float4*)x, (uint4*)y, n_chunks, H, g.Hp, g.Wp, L, tab);
+  const long long cap = (long long)sms * 16;
+  const int blocks = (int)(n_tokens < cap ? n_tokens : cap);
+  rope_unrotate_f32_kernel<<<blocks, 128, 0, s>>>((const float4*)x, (uint4*)y, n_tokens, H, g.Hp, g.Wp, L, tab);
   return cudaGetLastError();
 }
 
@@ -96,20 +143,19 @@ cudaError_t launch_rope_rotate_bf16(const void* x, void* y, int B, wan_grid_t g,
 
 cudaError_t launch_rope_rotate_bf16_rows(const void* x, void* y, int B, int L, int pos0, wan_grid_t g, int H,
                                          RopeTables tab, bool inverse, cudaStream_t s) {
-  const long long n_chunks = (long long)B * L * H * (kHeadDim / 8);
-  if (n_chunks == 0) return cudaSuccess;
+  const long long n_tokens = (long long)B * L;
+  if (n_tokens == 0 || H == 0) return cudaSuccess;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  long long want = (n_chunks + 255) / 256;
-  long long cap = (long long)sms * 8;  // 8 resident blocks of 256 threads per SM
-  const int blocks = (int)(want < cap ? want : cap);
+  const long long cap = (long long)sms * 16;  // 16 resident blocks of 128 threads per SM
+  const int blocks = (int)(n_tokens < cap ? n_tokens : cap);
+  const uint4* xs = static_cast<const uint4*>(x);
+  uint4* ys = static_cast<uint4*>(y);
   if (inverse)
-    rope_rotate_kernel<true><<<blocks, 256, 0, s>>>((const uint4*)x, (uint4*)y, n_chunks, H, g.Hp, g.Wp, L, pos0,
-                                                     tab);
+    rope_rotate_kernel<true><<<blocks, 128, 0, s>>>(xs, ys, n_tokens, H, g.Hp, g.Wp, L, pos0, tab);
   else
-    rope_rotate_kernel<false><<<blocks, 256, 0, s>>>((const uint4*)x, (uint4*)y, n_chunks, H, g.Hp, g.Wp, L, pos0,
-                                                      tab);
+    rope_rotate_kernel<false><<<blocks, 128, 0, s>>>(xs, ys, n_tokens, H, g.Hp, g.Wp, L, pos0, tab);
   return cudaGetLastError();
 }
 

@@ -1,4 +1,6 @@
 """Shared helpers of the test suite: seeded inputs, conversions, comparison."""
+import contextlib
+import ctypes
 import math
 
 import numpy as np
@@ -94,3 +96,47 @@ def rows_whose_reference_moves(qf, kf, grid, bound=256.0):
                     moved |= need
                 moved_rows += int(moved.sum())
     return moved_rows
+
+
+@contextlib.contextmanager
+def blas_single_threaded():
+    """Run numpy's BLAS on one thread inside the block, so that a pool of
+    Python threads, each in its own BLAS call, spreads over the cores without
+    oversubscribing them. Uses threadpoolctl when installed, else the loaded
+    OpenBLAS's own set_num_threads; if neither is found, BLAS is left as is
+    (the result is the same, only slower)."""
+    try:
+        from threadpoolctl import threadpool_limits
+    except ImportError:
+        threadpool_limits = None
+    if threadpool_limits is not None:
+        with threadpool_limits(limits=1, user_api="blas"):
+            yield
+        return
+    setter = getter = None
+    try:
+        with open("/proc/self/maps") as f:
+            paths = sorted({ln.split()[-1] for ln in f if "openblas" in ln.lower() and ln.split()[-1].startswith("/")})
+        for path in paths:
+            lib = ctypes.CDLL(path)
+            for suffix in ("64_", ""):
+                for prefix in ("scipy_openblas", "openblas"):
+                    if hasattr(lib, f"{prefix}_set_num_threads{suffix}"):
+                        setter = getattr(lib, f"{prefix}_set_num_threads{suffix}")
+                        getter = getattr(lib, f"{prefix}_get_num_threads{suffix}")
+                        break
+                if setter:
+                    break
+            if setter:
+                break
+    except OSError:
+        setter = None
+    if setter is None:
+        yield
+        return
+    before = int(getter())
+    setter(1)
+    try:
+        yield
+    finally:
+        setter(before)

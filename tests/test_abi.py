@@ -127,6 +127,14 @@ def test_tables_reject_bad_arguments(lib):
     assert wan.wan_rope3d_tables((3, 8, 8), 100, 1e4, FAKE, 0) == wan.WAN_ERR_UNSUPPORTED
 
 
+def test_profile_pass_hook_argument_checks(lib):
+    assert lib.wan_profile_set_pass_events(4, None, None) == wan.WAN_ERR_INVALID
+    assert lib.wan_profile_set_pass_events(-1, None, None) == wan.WAN_ERR_INVALID
+    assert lib.wan_profile_set_pass_events(wan.WAN_PASS_ROPE, 1, None) == wan.WAN_ERR_INVALID
+    for p in (wan.WAN_PASS_MAIN, wan.WAN_PASS_ROPE, wan.WAN_PASS_ROWS, wan.WAN_PASS_POST):
+        assert lib.wan_profile_set_pass_events(p, None, None) == wan.WAN_OK
+
+
 def test_debug_hook_argument_checks(lib):
     assert wan.wan_debug_inject_stall(-1, 10) == wan.WAN_ERR_INVALID
     assert wan.wan_debug_inject_stall(1, 0) == wan.WAN_ERR_INVALID

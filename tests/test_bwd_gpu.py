@@ -78,15 +78,25 @@ def test_backward_exhaustive_16x32x32():
     compare(dev_to_f64(dv), dv_r, "dV")
 
 
-def test_training_step_full_size_sampled():
-    """64x64x64 grid, H = 12: O, LSE and dQ on 4096 sampled rows against the
-    oracle; dK and dV through the exact sum identities on every head."""
+@pytest.fixture(scope="module")
+def full_step():
+    """The 64x64x64 grid, H = 12 training step (forward, then backward on the
+    forward's O and LSE), run once for the full-size tests below."""
     from long_sequence_attention_02_b300.workloads import WORKLOADS
 
     w = WORKLOADS["train_64x64x64_fwd_bwd"]
+    qb, kb, vb, dob = _inputs(w.B, w.grid, w.H, seed=0)
+    out = _run(qb, kb, vb, dob, w.grid)
+    yield w, (qb, kb, vb, dob), out
+    del out
+    torch.cuda.empty_cache()
+
+
+def test_training_step_full_size_sampled(full_step):
+    """O, LSE and dQ on 4096 sampled rows against the oracle; dK and dV
+    through the exact sum identities on every head."""
+    w, (qb, kb, vb, dob), (o, lse, dq, dk, dv) = full_step
     B, L, H, grid = w.B, w.L, w.H, w.grid
-    qb, kb, vb, dob = _inputs(B, grid, H, seed=0)
-    o, lse, dq, dk, dv = _run(qb, kb, vb, dob, grid)
     rng = np.random.default_rng(3)
     flat = rng.choice(B * H * L, size=4096, replace=False)
     bs, hs, is_ = flat // (H * L), (flat // L) % H, flat % L
@@ -111,3 +121,27 @@ def test_training_step_full_size_sampled():
         dkr = ref.rope_rotate(dev_to_f64(dk[0, :, h]), ang)
         col = dkr.sum(axis=0)
         assert np.abs(col).max() < 2e-2 * np.abs(dkr).sum(axis=0).max() + 1e-3
+
+
+def test_training_step_full_size_key_rows(full_step):
+    """dK and dV element by element on 4096 seeded key rows of one seeded head
+    of the 262,144-token step. Each key row needs the LSE and D of all
+    262,144 queries of its head, so the oracle runs that head's whole forward
+    (in blocks of query rows spread over the host's cores) and then the
+    selected key columns of the backward."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    from tests._util import blas_single_threaded
+
+    w, (qb, kb, vb, dob), (_, _, _, dk, dv) = full_step
+    B, L, H, grid = w.B, w.L, w.H, w.grid
+    rng = np.random.default_rng(29)
+    b, h = int(rng.integers(B)), int(rng.integers(H))
+    keys = np.sort(rng.choice(L, size=4096, replace=False))
+    heads = [f64(x[b, :, h]) for x in (qb, kb, vb, dob)]
+    workers = max(1, min(len(os.sched_getaffinity(0)), 32))
+    with blas_single_threaded(), ThreadPoolExecutor(workers) as ex:
+        dk_r, dv_r = ref.self_attention_bwd_dkdv_rows(*heads, keys, grid, block=64, row_map=ex.map)
+    compare(dev_to_f64(dk[b, keys, h]), dk_r, f"dK (head {h}, 4096 key rows)")
+    compare(dev_to_f64(dv[b, keys, h]), dv_r, f"dV (head {h}, 4096 key rows)")

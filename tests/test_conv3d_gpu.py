@@ -104,3 +104,29 @@ def test_conv3d_full_size_sampled():
     ref = vae.causal_conv3d_at(f64(x), f64(wt), bias.astype(np.float64), f64(cache), pos)
     compare(got, ref, "y (sampled)")
     assert np.array_equal(dev_to_f64(co), f64(x[:, -2:])), "next cache"
+
+
+def test_conv3d_timed_layer_sampled():
+    """The layer the benchmark times (4 frames of 360 x 640, 192 -> 192
+    channels, with a cache: 45 x 40 output patches of 8 x 16 per frame) on
+    512 seeded sampled positions plus the corners and the edges of the last
+    patch row and column."""
+    from long_sequence_attention_02_b300.workloads import CONV_WORKLOADS
+
+    w = CONV_WORKLOADS["wan_vae_conv3d_360x640_192"]
+    x, cache, wt, bias = _layer(26, w.B, w.T, w.H, w.W, w.c_in, w.c_out, True, True)
+    y, co = _run(x, cache, wt, bias)
+    rng = np.random.default_rng(27)
+    n = 512
+    pos = list(zip(rng.integers(0, w.B, n), rng.integers(0, w.T, n), rng.integers(0, w.H, n),
+                   rng.integers(0, w.W, n)))
+    T, H, W = w.T, w.H, w.W
+    edges = [(0, 0, 0, 0), (0, T - 1, H - 1, W - 1), (0, 0, H - 1, 0), (0, T - 1, 0, W - 1),
+             (0, 1, H - 8, W - 16), (0, 2, H - 1, W - 17), (0, 3, H - 9, W - 1), (0, 0, 7, 15), (0, 0, 8, 16)]
+    edges += [(0, t, H - 1, int(c)) for t in range(T) for c in rng.integers(0, W, 8)]
+    edges += [(0, t, int(r), W - 1) for t in range(T) for r in rng.integers(0, H, 8)]
+    pos = edges + pos
+    got = dev_to_f64(torch.stack([y[p] for p in pos]))
+    ref = vae.causal_conv3d_at(f64(x), f64(wt), bias.astype(np.float64), f64(cache), pos)
+    compare(got, ref, "y (timed layer, sampled)")
+    assert np.array_equal(dev_to_f64(co), f64(x[:, -2:])), "next cache"

@@ -92,3 +92,27 @@ def test_timeout_in_fp8_forward():
     # the FP8 tolerance (derived in test_fp8_gpu.py): relative L2 0.12 on O, LSE max-abs 0.2
     compare(dev_to_f64(o), o_ref, "fp8 O after recovery", max_abs=0.15 * float(np.abs(o_ref).max()), rel_l2=0.12)
     compare(dev_to_f64(lse), lse_ref, "fp8 LSE after recovery", max_abs=0.2, rel_l2=float("inf"))
+
+
+def test_timeout_in_conv3d():
+    """The VAE Conv3d producer withholds one K step: the MMA warp's bounded
+    wait expires, the epilogue skips its stores, TMEM is freed, and the next
+    call is correct."""
+    from oracle import vae
+    from tests._util import bf16_round
+
+    B, T, H, W, c_in, c_out = 1, 2, 8, 16, 64, 128
+    x = bits(11, synth.STREAM_Q, (B, T, H, W, c_in))
+    wt = bf16_round(f64(bits(11, synth.STREAM_V, (c_out, 3, 3, 3, c_in))) * 2.0 ** -5)
+    xd, wd = to_dev(x), to_dev(wt)
+    y = torch.empty(B, T, H, W, c_out, dtype=torch.bfloat16, device="cuda")
+    wan.check(wan.wan_debug_inject_stall(1, 100))
+    try:
+        wan.check(wan.wan_vae_causal_conv3d(xd, None, wd, None, y, None, B, T, H, W, c_in, c_out))
+    finally:
+        wan.wan_debug_inject_stall(0, 100)
+    assert wan.wan_get_device_status() == wan.WAN_ERR_TIMEOUT
+    wan.check(wan.wan_vae_causal_conv3d(xd, None, wd, None, y, None, B, T, H, W, c_in, c_out))
+    assert wan.wan_get_device_status() == wan.WAN_OK
+    y_ref, _ = vae.causal_conv3d(f64(x), f64(wt))
+    compare(dev_to_f64(y), y_ref, "conv3d y after recovery")

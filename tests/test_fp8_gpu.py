@@ -13,6 +13,27 @@ Tolerance (no precision is stated for FP8, so it is derived here). e4m3 keeps 3 
 - LSE. It uses the fp32 probabilities, so it carries only the logit error: a p-weighted mean of
   errors whose RMS is ~0.05 for N(0,1) inputs. A row with one key (or one dominant key) keeps
   that error whole, with no averaging. Bound: 4 RMS = 0.2.
+
+A second, tight comparison is against the quantised oracle (oracle.fp8): the same per-head e4m3
+quantisation of the rotated Q, K and of V, then the exact fp64 softmax. What separates it from the
+kernel is only P's e4m3 rounding (for the P V product) and fp32 arithmetic. Its bounds, derived from
+that rounding alone (and not adjusted to measurements):
+- Write pi_j for the softmax weights, so O_id = sum_j pi_j v_jd. A probability in e4m3's normal range
+  (p >= 2^-6 on the kernel's own scale, where the largest p of the first key tile is 1) is rounded
+  with relative error |delta| <= 2^-4; taken as uniform, E[delta^2] <= 2^-8/3 (RMS 0.0361). Below
+  2^-6 the absolute error is at most 2^-10, half the subnormal spacing.
+- The error of O_id is a sum of independent terms pi_j delta_j v_jd, so its variance is
+  sigma_id^2 = (2^-8/3) sum_j pi_j^2 v_jd^2 + (2^-20/3) sum_j v_jd^2 / l^2, where the kernel's
+  l = sum_j p_j is at least exp(LSE_i - max_j s_ij). Element-wise bound: 8 sigma_id, plus 2^-8 |O|
+  for the bf16 output.
+- Relative L2 of O. With V independent of the weights, E|O_id|^2 = sum_j pi_j^2 E v^2, so the
+  normal-range term gives rel-L2 <= sqrt(2^-8/3) = 0.0361; the subnormal term and the bf16 output
+  (2^-8/sqrt(3)) add under a percent of that in quadrature. Bound: 0.04.
+- LSE uses the unrounded fp32 probabilities: only fp32 arithmetic separates it from the quantised
+  oracle, plus the rare input element whose fp32 and fp64 quantisations land on either side of an
+  e4m3 midpoint (a shift of a few 1e-3 in that row's logits). Bound: 2e-2, the workload's bf16 one.
+- The same comparison fails for a scale off by 10 %: rel-L2 is then ~0.09 (s_v) or ~0.15 (s_q s_k);
+  the tests check that on the host with perturbed reference scales.
 """
 import math
 
@@ -21,7 +42,7 @@ import pytest
 
 import long_sequence_attention_02_b300 as wan
 from long_sequence_attention_02_b300 import synth
-from oracle import ref
+from oracle import fp8, ref
 from tests._util import bf16_round, bits, compare, dev_to_f64, f64, rows_whose_reference_moves, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -30,12 +51,61 @@ torch = pytest.importorskip("torch")
 FP8_REL_L2 = 0.12
 FP8_MAX_ABS_FRACTION = 0.15  # of max |O_ref|
 FP8_LSE_MAX_ABS = 0.2
+# against the quantised oracle
+FP8Q_REL_L2 = 0.04
+FP8Q_SIGMAS = 8.0
+FP8Q_LSE_MAX_ABS = 2e-2
 
 
 def compare_fp8(o, o_ref, lse, lse_ref, name):
     compare(o, o_ref, f"O ({name})", max_abs=FP8_MAX_ABS_FRACTION * float(np.abs(o_ref).max()), rel_l2=FP8_REL_L2)
     # LSE is judged by its absolute error: with one key it is a single logit, which can be near 0.
     compare(lse, lse_ref, f"LSE ({name})", max_abs=FP8_LSE_MAX_ABS, rel_l2=float("inf"))
+
+
+def quantised_reference(qd, kd, vd, rows=None, logit_gain=1.0):
+    """O, LSE and the per-element error scale sigma of the quantised oracle
+    for one head whose dequantised operands are qd, kd, vd [L, d] (query
+    rows `rows` only, if given)."""
+    sc = logit_gain / math.sqrt(qd.shape[1])
+    qs = qd if rows is None else qd[rows]
+    o, lse = ref.softmax_attention(qs, kd, vd, sc)
+    # sum_j pi_j^2 v_jd^2 = exp(LSE2 - 2 LSE) * (softmax at twice the logits applied to v^2)
+    o2, lse2 = ref.softmax_attention(qs, kd, vd * vd, 2 * sc)
+    normal = (2.0 ** -8 / 3) * np.exp(lse2 - 2 * lse)[:, None] * o2
+    s_max = np.max(sc * (qs @ kd.T), axis=1)
+    sub = (2.0 ** -20 / 3) * np.exp(2 * (s_max - lse))[:, None] * np.sum(vd * vd, axis=0)[None, :]
+    return o, lse, np.sqrt(normal + sub)
+
+
+def compare_fp8_quantised(o, lse, o_q, lse_q, sigma, name):
+    """The tight comparison (bounds derived in the module docstring)."""
+    err = np.abs(o - o_q)
+    bound = FP8Q_SIGMAS * sigma + 2.0 ** -8 * np.abs(o_q) + 1e-6
+    worst = np.unravel_index(np.argmax(err / bound), err.shape)
+    assert np.all(err <= bound), (f"O ({name}): error {err[worst]:.3e} > bound {bound[worst]:.3e} "
+                                  f"at {worst}")
+    compare(o, o_q, f"O ({name}, quantised oracle)", max_abs=float(bound.max()), rel_l2=FP8Q_REL_L2)
+    compare(lse, lse_q, f"LSE ({name}, quantised oracle)", max_abs=FP8Q_LSE_MAX_ABS, rel_l2=float("inf"))
+
+
+def _rel_l2(a, b):
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+def check_quantised_every_row(o, lse, qb, kb, vb, grid, name, perturb=False):
+    """Every row of every head against the quantised oracle; with perturb,
+    also show that a 10 % error in s_v or in s_q s_k would fail the bound."""
+    B, L, H, _ = qb.shape
+    for b in range(B):
+        for h in range(H):
+            qd, kd, vd = fp8.head_operands(f64(qb[b, :, h]), f64(kb[b, :, h]), f64(vb[b, :, h]), grid)
+            o_q, lse_q, sig = quantised_reference(qd, kd, vd)
+            compare_fp8_quantised(o[b, :, h], lse[b, h], o_q, lse_q, sig, f"{name}, b{b} h{h}")
+            if perturb:
+                assert _rel_l2(o[b, :, h], 1.1 * o_q) > FP8Q_REL_L2       # s_v 10 % high
+                o_g, _, _ = quantised_reference(qd, kd, vd, logit_gain=1.1)  # s_q s_k 10 % high
+                assert _rel_l2(o[b, :, h], o_g) > FP8Q_REL_L2
 
 
 def _inputs(B, grid, H, seed):
@@ -62,6 +132,7 @@ def test_fp8_every_row(B, grid, H):
     o, lse = _run(qb, kb, vb, grid)
     o_ref, lse_ref = ref.self_attention_fwd(f64(qb), f64(kb), f64(vb), grid)
     compare_fp8(o, o_ref, lse, lse_ref, "fp8")
+    check_quantised_every_row(o, lse, qb, kb, vb, grid, "fp8", perturb=grid[0] * grid[1] * grid[2] >= 192)
 
 
 def test_fp8_zero_queries_give_mean_values():
@@ -89,6 +160,7 @@ def test_fp8_reference_moves():
     o, lse = _run(qb, kb, vb, grid)
     o_ref, lse_ref = ref.self_attention_fwd(f64(qb), f64(kb), f64(vb), grid)
     compare_fp8(o, o_ref, lse, lse_ref, "fp8, moving reference")
+    check_quantised_every_row(o, lse, qb, kb, vb, grid, "fp8, moving reference")
 
 
 def test_fp8_tracks_the_bf16_path():
@@ -120,3 +192,12 @@ def test_fp8_full_size_sampled():
         r_o[sel], r_l[sel] = ref.self_attention_fwd_rows(f64(qb[bh[0], is_[sel], bh[1]]), is_[sel],
                                                          f64(kb[bh[0], :, bh[1]]), f64(vb[bh[0], :, bh[1]]), grid)
     compare_fp8(o_rows, r_o, lse_rows, r_l, "fp8, 75,600 tokens")
+    # the quantised oracle: each sampled head's scales come from all its rows
+    q_o, q_l, q_s = np.zeros_like(o_rows), np.zeros_like(lse_rows), np.zeros_like(o_rows)
+    for bh in sorted(set(zip(bs.tolist(), hs.tolist()))):
+        sel = np.where((bs == bh[0]) & (hs == bh[1]))[0]
+        qd, kd, vd = fp8.head_operands(f64(qb[bh[0], :, bh[1]]), f64(kb[bh[0], :, bh[1]]), f64(vb[bh[0], :, bh[1]]),
+                                       grid)
+        q_o[sel], q_l[sel], q_s[sel] = quantised_reference(qd, kd, vd, rows=is_[sel])
+    compare_fp8_quantised(o_rows, lse_rows, q_o, q_l, q_s, "fp8, 75,600 tokens")
+    assert _rel_l2(o_rows, 1.1 * q_o) > FP8Q_REL_L2

@@ -116,6 +116,32 @@ def test_decoupled_cross_attention(lens_txt, Lk_txt, lens_img, Lk_img):
     compare(dev_to_f64(lse), lse_ref, "LSE (text path)")
 
 
+@pytest.mark.parametrize("lens_txt,lens_img", [([300, 512], [257, 129]), ([512, 17], [0, 200])])
+def test_decoupled_cross_attention_many_items_every_row(lens_txt, lens_img):
+    """More work items than CTAs (2 batch items x 20 heads x 24 pairs of
+    query tiles = 960 items on 148 SMs): each CTA walks about six items, so
+    every Q buffer, O staging area and old-O load of the summed path is
+    reused several times; every row is compared. The second case has a batch
+    item with no image key (its items are skipped by the summed path)."""
+    grid, B, H = (6, 25, 40), 2, 20
+    Lq, Lt, Li = 6000, 512, 257
+    qb = bits(43, synth.STREAM_Q, (B, Lq, H, 128))
+    ktb, vtb = bits(43, synth.STREAM_K, (B, Lt, H, 128)), bits(43, synth.STREAM_V, (B, Lt, H, 128))
+    kib, vib = bits(44, synth.STREAM_K, (B, Li, H, 128)), bits(44, synth.STREAM_V, (B, Li, H, 128))
+    q = to_dev(qb)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, Lq, dtype=torch.float32, device="cuda")
+    lt = torch.tensor(lens_txt, dtype=torch.int32, device="cuda")
+    li = torch.tensor(lens_img, dtype=torch.int32, device="cuda")
+    wan.check(wan.wan_xattn_fwd_dual(q, to_dev(ktb), to_dev(vtb), lt, Lt, to_dev(kib), to_dev(vib), li, Li, o, lse,
+                                     B, grid, H, 128, 1 / math.sqrt(128)), "dual")
+    wan.check(wan.wan_get_device_status())
+    o_ref, lse_ref = ref.decoupled_cross_attention_fwd(f64(qb), f64(ktb), f64(vtb), lens_txt, f64(kib), f64(vib),
+                                                       lens_img)
+    compare(dev_to_f64(o), o_ref, "O (text + image, many items)")
+    compare(dev_to_f64(lse), lse_ref, "LSE (text path, many items)")
+
+
 # ---------------------------------------------------------------------------
 # Full-size cases on 4096 seeded sampled rows
 
