@@ -19,21 +19,28 @@
 //        dS^T = scale * P^T o (dP^T - D)                (threads, into TMEM + smem)
 //        dK  += dS^T Q_rot                              (A = dS^T from TMEM)
 //        dQ_i = dS K_rot  (two N=64 halves)             (A = dS from smem, MN-major)
-//      The dQ warpgroup reads dQ_i out of TMEM, stages it in the dS buffer
-//      (once the dQ MMA has read dS) as 128B-swizzled 128 x 32-float boxes,
-//      and adds it into the fp32 accumulator with bulk tensor reductions.
+//      The dQ warpgroup reads dQ_i out of TMEM and stages it, as 128B-swizzled
+//      128 x 32-float boxes, in the query tile's own {Q_rot, dO} stage: once
+//      the dQ MMA is done, every MMA that reads that stage is done too (the
+//      dQ MMAs come last in issue order), so d-half 0 goes where Q_rot was
+//      and d-half 1 where dO was. A reduction warp adds the staged halves
+//      into the fp32 accumulator with bulk tensor reductions and hands each
+//      slot back to the producer as soon as its reduction has read it.
 //      TMEM: dV [0,128) dK [128,256) S [256,384) dP [384,512); P^T, dS^T
 //      (bf16) and the dQ halves reuse S and dP columns once the MMAs that read
 //      them are ordered before (tcgen05 MMAs of one thread run in order).
 //      Epilogue: dV -> bf16; dK -> R^T -> bf16.
 //   3. post: dQ = R^T dQ_acc -> bf16.
 //      The fp32 reduction of dQ into global memory is the costly part of the
-//      backward (one 64 KB tile per query tile per CTA); it is done by a
-//      warpgroup of its own so that it overlaps the next tile's softmax.
+//      backward (one 64 KB tile per query tile per CTA, bound by the L2's
+//      reduction rate). Staging it in the consumed stage, instead of a buffer
+//      that the next tile's dS must wait for, lets one tile's reduction run
+//      under the next tile's MMAs and softmax; what it still gates is the
+//      next-but-one tile's Q_rot and dO loads into that stage.
 // Warps (register budgets moved with setmaxnreg):
 //   0-7    compute (warp w: TMEM lanes 32*(w%4).., column half w/4)   152 regs
 //   8      TMA producer; 9 MMA issuer (warp-converged, one elected lane
-//          issues) and TMEM owner; 10-11 idle                           112 regs
+//          issues) and TMEM owner; 10 dQ reductions; 11 idle            112 regs
 //   12-15  dQ writers (warp w: TMEM lanes 32*(w%4)..)                    96 regs
 #include "common.cuh"
 #include "kernels.cuh"
@@ -49,6 +56,7 @@ constexpr uint32_t kDqRegs = 96;
 constexpr int kDqWarp0 = 12;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kReduceWarp = 10;
 constexpr int kTile = 128;
 constexpr int kTileBytes = 128 * 128 * 2;
 constexpr int kHalfBytes = kTileBytes / 2;
@@ -65,8 +73,8 @@ constexpr int kSmemBytes = kOffBar + 256;  // barriers, TMEM base, abort word; d
 
 enum Bar {
   kBarKV = 0,
-  kBarQFull0 = 1,   // +stage
-  kBarQEmpty0 = 3,  // +stage
+  kBarQFull0 = 1,   // +stage: Q_rot tile and the rows {LSE*log2e, D} landed
+  kBarQEmpty0 = 3,  // +stage: the Q_rot slot (dQ half 0 staging) has been read by its reduction
   kBarS = 5,
   kBarDP = 6,
   kBarP = 7,
@@ -75,10 +83,13 @@ enum Bar {
   kBarDQFree0 = 10,  // ... and has been read: S of the next tile may be written
   kBarAcc = 11,
   kBarDrain = 12,
-  kBarDSFree = 13,  // the dS buffer, used as dQ staging after the dQ MMA, is free again
-  kBarDQ1 = 14,      // dQ half 1 (d 64..127) is in TMEM (dP columns 64..127)
-  kBarDQFree1 = 15,  // ... and has been read: dP of the next tile may be written
-  kNumBars = 16
+  kBarDQ1 = 13,      // dQ half 1 (d 64..127) is in TMEM (dP columns 64..127)
+  kBarDQFree1 = 14,  // ... and has been read: dP of the next tile may be written
+  kBarDOFull0 = 15,  // +stage: dO tile landed
+  kBarDOEmpty0 = 17,  // +stage: the dO slot (dQ half 1 staging) has been read by its reduction
+  kBarStaged0 = 19,  // +stage: dQ half 0 written into the stage's Q_rot slot
+  kBarStaged1 = 21,  // +stage: dQ half 1 written into the stage's dO slot
+  kNumBars = 23
 };
 static_assert(kNumBars * 8 + 8 <= 192, "barrier area overlaps the dQ stop flags");
 
@@ -148,6 +159,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars[kBarQFull0 + s], 1);
       mbar_init(&bars[kBarQEmpty0 + s], 1);
+      mbar_init(&bars[kBarDOFull0 + s], 1);
+      mbar_init(&bars[kBarDOEmpty0 + s], 1);
+      mbar_init(&bars[kBarStaged0 + s], 4);  // one arrival per dQ warp
+      mbar_init(&bars[kBarStaged1 + s], 4);
     }
     mbar_init(&bars[kBarS], 1);
     mbar_init(&bars[kBarDP], 1);
@@ -159,7 +174,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kBarDQFree1], 4);
     mbar_init(&bars[kBarAcc], 1);
     mbar_init(&bars[kBarDrain], 1);
-    mbar_init(&bars[kBarDSFree], 1);
     *abort_sh = 0;
     fence_mbar_init();
   }
@@ -189,7 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_4d(smem + kOffK + kHalfBytes, &tm_k, &bars[kBarKV], 64, h, kv0, b);
       tma_load_4d(smem + kOffV, &tm_v, &bars[kBarKV], 0, h, kv0, b);
       tma_load_4d(smem + kOffV + kHalfBytes, &tm_v, &bars[kBarKV], 64, h, kv0, b);
-      int issued[2] = {0, 0};
+      // Stage s holds query tile i = s, s + 2, ...; each of its two slots is
+      // refilled as soon as the reduction of the dQ half staged in it has read it.
+      int issued_q[2] = {0, 0}, issued_do[2] = {0, 0};
       for (int i = 0; i < nq; ++i) {
         const int s = i & 1, use = i >> 1;
         if (use > 0 && !mbar_wait(&bars[kBarQEmpty0 + s], (use - 1) & 1, abort, to)) {
@@ -199,21 +215,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a.lc.stall && i == 1) continue;  // test hook: query tile 1 never arrives
         uint8_t* st = smem + kOffStage + s * kStageBytes;
         uint8_t* rows = smem + kOffRows + s * kRowsBytes;
-        uint64_t* bar = &bars[kBarQFull0 + s];
-        mbar_arrive_expect_tx(bar, 2 * kTileBytes + kRowsBytes);
         const int q0 = (i + q_start < nq ? i + q_start : i + q_start - nq) * kTile;
+        uint64_t* bar = &bars[kBarQFull0 + s];
+        mbar_arrive_expect_tx(bar, kTileBytes + kRowsBytes);
         tma_load_4d(st, &tm_q, bar, 0, h, q0, b);
         tma_load_4d(st + kHalfBytes, &tm_q, bar, 64, h, q0, b);
-        tma_load_4d(st + kTileBytes, &tm_do, bar, 0, h, q0, b);
-        tma_load_4d(st + kTileBytes + kHalfBytes, &tm_do, bar, 64, h, q0, b);
         bulk_load(rows, a.lse2 + bh * a.Lpad + q0, kTile * 4, bar);
         bulk_load(rows + kTile * 4, a.drow + bh * a.Lpad + q0, kTile * 4, bar);
-        issued[s] = use + 1;
+        issued_q[s] = use + 1;
+        if (use > 0 && !mbar_wait(&bars[kBarDOEmpty0 + s], (use - 1) & 1, abort, to)) {
+          raise_abort(abort, a.lc.err);
+          break;
+        }
+        bar = &bars[kBarDOFull0 + s];
+        mbar_arrive_expect_tx(bar, kTileBytes);
+        tma_load_4d(st + kTileBytes, &tm_do, bar, 0, h, q0, b);
+        tma_load_4d(st + kTileBytes + kHalfBytes, &tm_do, bar, 64, h, q0, b);
+        issued_do[s] = use + 1;
       }
       // Every copy this warp issued lands before the CTA may exit.
       mbar_wait(&bars[kBarKV], 0, nullptr, to);
-      for (int s = 0; s < 2; ++s)
-        if (issued[s] > 0) mbar_wait(&bars[kBarQFull0 + s], (issued[s] - 1) & 1, nullptr, to);
+      for (int s = 0; s < 2; ++s) {
+        if (issued_q[s] > 0) mbar_wait(&bars[kBarQFull0 + s], (issued_q[s] - 1) & 1, nullptr, to);
+        if (issued_do[s] > 0) mbar_wait(&bars[kBarDOFull0 + s], (issued_do[s] - 1) & 1, nullptr, to);
+      }
     }
     __syncwarp();
    } else if (warp == kMmaWarp) {
@@ -243,7 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ss_elect(tS, dK + off, dStage_k + so + off, id_kk, kk > 0);
         }
         umma_commit_elect(&bars[kBarS]);
+        if (!(ok = warp_wait(&bars[kBarDOFull0 + s], use & 1, abort, a.lc.err, to))) break;
         if (i > 0 && !(ok = warp_wait(&bars[kBarDQFree1], (i - 1) & 1, abort, a.lc.err, to))) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
@@ -273,12 +300,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                           dKmn + static_cast<uint64_t>((half * kHalfBytes + kk * 2048) >> 4), id_dq, kk > 0);
           umma_commit_elect(&bars[half ? kBarDQ1 : kBarDQ0]);
         }
-        umma_commit_elect(&bars[kBarQEmpty0 + s]);
       }
       if (ok) umma_commit_elect(&bars[kBarAcc]);
       umma_commit_elect(&bars[kBarDrain]);
       mbar_wait(&bars[kBarDrain], 0, nullptr, to);
     }
+   } else if (warp == kReduceWarp) {
+    // ------------------------------------------------------------ dQ reductions
+    // Adds each staged dQ half into the fp32 accumulator (two 128 x 32-float
+    // boxes per half) and returns its slot to the producer once the bulk copy
+    // has read it.
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_dq);
+      for (int i = 0; i < nq; ++i) {
+        const int s = i & 1, use = i >> 1;
+        const int qt = i + q_start < nq ? i + q_start : i + q_start - nq;
+        uint8_t* st = smem + kOffStage + s * kStageBytes;
+        if (!mbar_wait(&bars[kBarStaged0 + s], use & 1, abort, to)) {
+          raise_abort(abort, a.lc.err);
+          break;
+        }
+        tma_reduce_add_4d(&tm_dq, st, 0, h, qt * kTile, b);
+        tma_reduce_add_4d(&tm_dq, st + kTile * 128, 32, h, qt * kTile, b);
+        bulk_commit_group();
+        if (!mbar_wait(&bars[kBarStaged1 + s], use & 1, abort, to)) {
+          raise_abort(abort, a.lc.err);
+          break;
+        }
+        tma_reduce_add_4d(&tm_dq, st + kTileBytes, 64, h, qt * kTile, b);
+        tma_reduce_add_4d(&tm_dq, st + kTileBytes + kTile * 128, 96, h, qt * kTile, b);
+        bulk_commit_group();
+        bulk_wait_group_read<1>();  // half 0's reductions have read the Q_rot slot
+        mbar_arrive(&bars[kBarQEmpty0 + s]);
+        bulk_wait_group_read<0>();
+        mbar_arrive(&bars[kBarDOEmpty0 + s]);
+      }
+      bulk_wait_group0();  // every reduction is complete before the CTA exits
+    }
+    __syncwarp();
    }
   } else if (warp >= kDqWarp0) {
     regs_shrink<kDqRegs>();
@@ -289,62 +348,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Per-warp stop flags (in the dynamic barrier area: a static __shared__
     // array would move the 1024-byte aligned dynamic base).
     volatile int* dq_fail = reinterpret_cast<volatile int*>(smem + kOffBar + 192);
+    // Row r of the 128 x 64-float half in v -> two 128B-swizzled boxes of 32 floats.
+    auto stage_half = [&](uint8_t* dst, const uint32_t (&v)[64]) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c)  // box c/8, 16-byte chunk c%8 of row r
+        *reinterpret_cast<uint4*>(dst + (c >> 3) * (kTile * 128) + sw128_offset(r, c & 7)) =
+            make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+      fence_proxy_async_smem();  // visible to the bulk copies that read it
+    };
     for (int i = 0; i < nq; ++i) {
+      const int s = i & 1;
       const bool ok = warp_wait(&bars[kBarDQ0], i & 1, abort, a.lc.err, to);
       // The four warps decide together whether to stop, so that none of
-      // them is left waiting at the named barriers below.
+      // them is left waiting at the named barrier.
       if (lane == 0) dq_fail[wq] = ok ? 0 : 1;
       named_bar_sync(1, 128);
       if (dq_fail[0] | dq_fail[1] | dq_fail[2] | dq_fail[3]) break;
       tc_fence_after();
-      // Both halves leave TMEM before any staging round trip, so the next
-      // tile's S and dP MMAs are held up only by two TMEM loads each. The
-      // staging area is the dS buffer, free once both dQ halves' MMAs (which
-      // read dS) have completed. Each half is staged as two 128-row x
-      // 32-float boxes in the 128-byte swizzled layout and added to the fp32
-      // accumulator by one elected thread with bulk tensor reductions.
-      const int qt = i + q_start < nq ? i + q_start : i + q_start - nq;
-      uint8_t* stage = smem + kOffDS;
+      // Each half leaves TMEM first (so the next tile's S or dP MMA waits only
+      // for two TMEM loads), then goes to its slot of this tile's stage: every
+      // MMA that read the stage completed before the dQ MMAs did.
+      uint8_t* st = smem + kOffStage + s * kStageBytes;
       uint32_t v[64];
       tmem_ld32(tS + lane_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
       tmem_ld32(tS + lane_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-      tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[64]>(&v[0]));
+      tmem_ld_wait_regs(v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarDQFree0]);
+      stage_half(st, v);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarStaged0 + s]);
       // dQ half 1 is committed right after half 0 with no wait in between;
-      // this wait ignores the abort flag so that all four warps reach the
-      // barriers below (a timeout still raises the error).
+      // this wait ignores the abort flag so that all four warps come back to
+      // the named barrier above (a timeout still raises the error).
       if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarDQ1], i & 1, nullptr, to)) && lane == 0)
         raise_abort(abort, a.lc.err);
       tc_fence_after();
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-#pragma unroll
-        for (int c = 0; c < 16; ++c)  // box c/8, 16-byte chunk c%8 of row r
-          *reinterpret_cast<uint4*>(stage + (c >> 3) * (kTile * 128) + sw128_offset(r, c & 7)) =
-              make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-        if (half == 0) {
-          tmem_ld32(tDP + lane_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-          tmem_ld32(tDP + lane_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-          tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[64]>(&v[0]));
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kBarDQFree1]);
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (warp == kDqWarp0 && lane == 0) {
-          tma_reduce_add_4d(&tm_dq, stage, half * 64, h, qt * kTile, b);
-          tma_reduce_add_4d(&tm_dq, stage + kTile * 128, half * 64 + 32, h, qt * kTile, b);
-          bulk_commit_group();
-          bulk_wait_group_read0();
-          if (half == 1) mbar_arrive(&bars[kBarDSFree]);
-        }
-        named_bar_sync(1, 128);
-      }
+      tmem_ld32(tDP + lane_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(tDP + lane_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_ld_wait_regs(v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarDQFree1]);
+      stage_half(st + kTileBytes, v);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBarStaged1 + s]);
     }
-    if (warp == kDqWarp0 && lane == 0) bulk_wait_group0();
   } else {
     regs_grow<kComputeRegs>();
     // ------------------------------------------------------------ compute
@@ -413,11 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st32(tDP + lane_addr + ch * 64, pk);
         // dS^T row r, queries ch*64 .. ch*64+63 -> half tile ch of the MN-major A operand.
-        // The dS buffer doubles as the dQ staging area of the previous tile.
-        if (i > 0 && !(ok = warp_wait(&bars[kBarDSFree], (i - 1) & 1, abort, a.lc.err, to))) {
-          tmem_st_wait();
-          break;
-        }
+        // The previous tile's dQ MMAs, the last readers of the dS buffer, were
+        // issued before this tile's dP MMA, so they completed before DP fired.
         uint8_t* ds_row = smem + kOffDS + ch * kHalfBytes;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc)
