@@ -40,8 +40,8 @@
 // Warps (register budgets moved with setmaxnreg):
 //   0-7    compute (warp w: TMEM lanes 32*(w%4).., column half w/4)   152 regs
 //   8      TMA producer; 9 MMA issuer (warp-converged, one elected lane
-//          issues) and TMEM owner; 10 dQ reductions; 11 idle            112 regs
-//   12-15  dQ writers (warp w: TMEM lanes 32*(w%4)..)                    96 regs
+//          issues) and TMEM owner; 10 dQ reductions; 11 idle             96 regs
+//   12-15  dQ writers (warp w: TMEM lanes 32*(w%4)..)                   112 regs
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -50,9 +50,9 @@ namespace wan {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr uint32_t kComputeRegs = 152;  // 2 x 128 x 152 + 128 x 112 + 128 x 96 = 512 x 128
-constexpr uint32_t kControlRegs = 112;
-constexpr uint32_t kDqRegs = 96;
+constexpr uint32_t kComputeRegs = 152;  // 2 x 128 x 152 + 128 x 96 + 128 x 112 = 512 x 128
+constexpr uint32_t kControlRegs = 96;
+constexpr uint32_t kDqRegs = 112;
 constexpr int kDqWarp0 = 12;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -79,17 +79,15 @@ enum Bar {
   kBarDP = 6,
   kBarP = 7,
   kBarDS = 8,
-  kBarDQ0 = 9,       // dQ half 0 (d 0..63) is in TMEM (S columns 64..127)
-  kBarDQFree0 = 10,  // ... and has been read: S of the next tile may be written
+  kBarDQ = 9,       // dQ (128 x 128 fp32) is in TMEM (dP columns)
+  kBarDQFree = 10,  // ... and has been read: dP of the next tile may be written
   kBarAcc = 11,
   kBarDrain = 12,
-  kBarDQ1 = 13,      // dQ half 1 (d 64..127) is in TMEM (dP columns 64..127)
-  kBarDQFree1 = 14,  // ... and has been read: dP of the next tile may be written
-  kBarDOFull0 = 15,  // +stage: dO tile landed
-  kBarDOEmpty0 = 17,  // +stage: the dO slot (dQ half 1 staging) has been read by its reduction
-  kBarStaged0 = 19,  // +stage: dQ half 0 written into the stage's Q_rot slot
-  kBarStaged1 = 21,  // +stage: dQ half 1 written into the stage's dO slot
-  kNumBars = 23
+  kBarDOFull0 = 13,  // +stage: dO tile landed
+  kBarDOEmpty0 = 15,  // +stage: the dO slot (dQ half 1 staging) has been read by its reduction
+  kBarStaged0 = 17,  // +stage: dQ half 0 written into the stage's Q_rot slot
+  kBarStaged1 = 19,  // +stage: dQ half 1 written into the stage's dO slot
+  kNumBars = 21
 };
 static_assert(kNumBars * 8 + 8 <= 192, "barrier area overlaps the dQ stop flags");
 
@@ -168,10 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[kBarDP], 1);
     mbar_init(&bars[kBarP], 8);
     mbar_init(&bars[kBarDS], 8);
-    mbar_init(&bars[kBarDQ0], 1);
-    mbar_init(&bars[kBarDQ1], 1);
-    mbar_init(&bars[kBarDQFree0], 4);
-    mbar_init(&bars[kBarDQFree1], 4);
+    mbar_init(&bars[kBarDQ], 1);
+    mbar_init(&bars[kBarDQFree], 4);
     mbar_init(&bars[kBarAcc], 1);
     mbar_init(&bars[kBarDrain], 1);
     *abort_sh = 0;
@@ -246,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       const uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);  // both operands K-major
       const uint32_t id_tm = idesc_bf16_f32(128, 128, 0, 1);  // A from TMEM, B MN-major
-      const uint32_t id_dq = idesc_bf16_f32(128, 64, 1, 1);   // A and B MN-major, N = 64
+      const uint32_t id_dq = idesc_bf16_f32(128, 128, 1, 1);  // A and B MN-major
       const uint64_t dK = sdesc_sw128(smem_u32(smem + kOffK), 16, 1024);
       const uint64_t dV = sdesc_sw128(smem_u32(smem + kOffV), 16, 1024);
       const uint64_t dKmn = sdesc_sw128(smem_u32(smem + kOffK), kHalfBytes, 1024);
@@ -258,8 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = i & 1, use = i >> 1;
         const uint64_t so = static_cast<uint64_t>((s * kStageBytes) >> 4);   // Q tile of stage s
         const uint64_t sdo = so + static_cast<uint64_t>(kTileBytes >> 4);      // dO tile of stage s
+        // S^T(i) goes into the S columns, whose last reader (dV(i-1)) was
+        // issued earlier: no wait on the dQ warps.
         ok = warp_wait(&bars[kBarQFull0 + s], use & 1, abort, a.lc.err, to);
-        if (ok && i > 0) ok = warp_wait(&bars[kBarDQFree0], (i - 1) & 1, abort, a.lc.err, to);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -269,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit_elect(&bars[kBarS]);
         if (!(ok = warp_wait(&bars[kBarDOFull0 + s], use & 1, abort, a.lc.err, to))) break;
-        if (i > 0 && !(ok = warp_wait(&bars[kBarDQFree1], (i - 1) & 1, abort, a.lc.err, to))) break;
+        // dP^T(i) goes into the dP columns once dQ(i-1) has been read out of them.
+        if (i > 0 && !(ok = warp_wait(&bars[kBarDQFree], (i - 1) & 1, abort, a.lc.err, to))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -290,16 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 8; ++kk)
           umma_ts_elect(tDK, tDP + (kk >> 2) * 64 + (kk & 3) * 8, dStage_mn + so + static_cast<uint64_t>(kk * 128),
                         id_tm, (i > 0 || kk > 0) ? 1u : 0u);
-        // dQ_i = dS K_rot, d-halves into S[64,128) and dP[64,128), each with
-        // its own commit so that the dQ warps can start on half 0 early.
+        // dQ_i = dS K_rot (N = 128) into the dP columns: the fp32 dP there has
+        // been read by the softmax, and the dS^T there by the dK MMAs issued
+        // just before (tcgen05 MMAs of one thread run in order).
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ss_elect((half ? tDP : tS) + 64, dDS + static_cast<uint64_t>(kk * 128),
-                          dKmn + static_cast<uint64_t>((half * kHalfBytes + kk * 2048) >> 4), id_dq, kk > 0);
-          umma_commit_elect(&bars[half ? kBarDQ1 : kBarDQ0]);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss_elect(tDP, dDS + static_cast<uint64_t>(kk * 128), dKmn + static_cast<uint64_t>((kk * 2048) >> 4),
+                        id_dq, kk > 0);
+        umma_commit_elect(&bars[kBarDQ]);
       }
       if (ok) umma_commit_elect(&bars[kBarAcc]);
       umma_commit_elect(&bars[kBarDrain]);
@@ -358,39 +354,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     for (int i = 0; i < nq; ++i) {
       const int s = i & 1;
-      const bool ok = warp_wait(&bars[kBarDQ0], i & 1, abort, a.lc.err, to);
+      const bool ok = warp_wait(&bars[kBarDQ], i & 1, abort, a.lc.err, to);
       // The four warps decide together whether to stop, so that none of
       // them is left waiting at the named barrier.
       if (lane == 0) dq_fail[wq] = ok ? 0 : 1;
       named_bar_sync(1, 128);
       if (dq_fail[0] | dq_fail[1] | dq_fail[2] | dq_fail[3]) break;
       tc_fence_after();
-      // Each half leaves TMEM first (so the next tile's S or dP MMA waits only
-      // for two TMEM loads), then goes to its slot of this tile's stage: every
-      // MMA that read the stage completed before the dQ MMAs did.
+      // Half 0 (d 0..63) is staged before half 1 leaves TMEM (the next tile's
+      // dP MMA waits for that). Each half goes to its slot of this tile's
+      // stage: every MMA that read the stage completed before the dQ MMAs did.
       uint8_t* st = smem + kOffStage + s * kStageBytes;
       uint32_t v[64];
-      tmem_ld32(tS + lane_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-      tmem_ld32(tS + lane_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_ld32(tDP + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(tDP + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tmem_ld_wait_regs(v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarDQFree0]);
       stage_half(st, v);
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarStaged0 + s]);
-      // dQ half 1 is committed right after half 0 with no wait in between;
-      // this wait ignores the abort flag so that all four warps come back to
-      // the named barrier above (a timeout still raises the error).
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars[kBarDQ1], i & 1, nullptr, to)) && lane == 0)
-        raise_abort(abort, a.lc.err);
-      tc_fence_after();
       tmem_ld32(tDP + lane_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
       tmem_ld32(tDP + lane_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tmem_ld_wait_regs(v);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarDQFree1]);
+      if (lane == 0) mbar_arrive(&bars[kBarDQFree]);
       stage_half(st + kTileBytes, v);
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarStaged1 + s]);
@@ -414,22 +401,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = warp_wait(&bars[kBarS], i & 1, abort, a.lc.err, to);
       if (!ok) break;
       tc_fence_after();
+      // P^T row of key r, queries ch*64 .. ch*64+63, two lanes of arithmetic
+      // per f32x2 instruction. Keys past the end (zero K rows) get P = 0: a
+      // warp decides once whether any of its keys is past the end.
       float p[64];
       {
-        float sv[32];
+        uint32_t sr[64];
+        tmem_ld32(tS + lane_addr + ch * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(tS + lane_addr + ch * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        tmem_ld_wait_regs(sr);
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          load32(tS + lane_addr + ch * 64 + c * 32, sv);
+        for (int k4 = 0; k4 < 16; ++k4) {  // the row values are the same for every lane: 16-byte broadcasts
+          const float4 l4 = reinterpret_cast<const float4*>(lse2)[k4];
+          const int k = 4 * k4;
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), sl2x2, f2_pack(-l4.x, -l4.y)),
+                    x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3])), sl2x2,
+                           f2_pack(-l4.z, -l4.w)),
+                    x2, x3);
+          p[k] = ex2_approx(x0);
+          p[k + 1] = ex2_approx(x1);
+          p[k + 2] = ex2_approx(x2);
+          p[k + 3] = ex2_approx(x3);
+        }
+        if (!__all_sync(0xffffffffu, key_ok) && !key_ok) {
 #pragma unroll
-          for (int k4 = 0; k4 < 8; ++k4) {  // the row values are the same for every lane: 16-byte broadcasts
-            const float4 l4 = reinterpret_cast<const float4*>(lse2)[c * 8 + k4];
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int k = 4 * k4 + e;
-              p[c * 32 + k] = key_ok ? ex2_approx(fmaf(sv[k], sl2, -lv[e])) : 0.f;
-            }
-          }
+          for (int k = 0; k < 64; ++k) p[k] = 0.f;
         }
       }
       {
@@ -447,18 +446,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       {
         uint32_t pk[32];
-        float dv[32];
+        // dS = scale * P o (dP - D), two lanes per f32x2 instruction, in two
+        // 32-column chunks.
+        const uint64_t sc2 = f2_pack(a.scale, a.scale);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          load32(tDP + lane_addr + ch * 64 + c * 32, dv);
+          uint32_t dr[32];
+          tmem_ld32(tDP + lane_addr + ch * 64 + c * 32, dr);
+          tmem_ld_wait_regs(dr);
 #pragma unroll
           for (int k4 = 0; k4 < 8; ++k4) {
             const float4 d4 = reinterpret_cast<const float4*>(drow)[c * 8 + k4];
-            const int j0 = c * 32 + 4 * k4;
-            pk[c * 16 + 2 * k4] = pack_bf16x2(p[j0] * (dv[4 * k4] - d4.x) * a.scale,
-                                              p[j0 + 1] * (dv[4 * k4 + 1] - d4.y) * a.scale);
-            pk[c * 16 + 2 * k4 + 1] = pack_bf16x2(p[j0 + 2] * (dv[4 * k4 + 2] - d4.z) * a.scale,
-                                                  p[j0 + 3] * (dv[4 * k4 + 3] - d4.w) * a.scale);
+            const int k = 4 * k4, j = c * 32 + k;
+            float s0, s1, s2, s3;
+            f2_unpack(f2_mul(f2_sub(f2_pack(__uint_as_float(dr[k]), __uint_as_float(dr[k + 1])), f2_pack(d4.x, d4.y)),
+                             f2_mul(f2_pack(p[j], p[j + 1]), sc2)),
+                      s0, s1);
+            f2_unpack(f2_mul(f2_sub(f2_pack(__uint_as_float(dr[k + 2]), __uint_as_float(dr[k + 3])),
+                                    f2_pack(d4.z, d4.w)),
+                             f2_mul(f2_pack(p[j + 2], p[j + 3]), sc2)),
+                      s2, s3);
+            pk[c * 16 + 2 * k4] = pack_bf16x2(s0, s1);
+            pk[c * 16 + 2 * k4 + 1] = pack_bf16x2(s2, s3);
           }
         }
         tmem_st32(tDP + lane_addr + ch * 64, pk);
