@@ -262,8 +262,10 @@ int wan_debug_inject_stall(int count, int timeout_ms);
  *     calls whose work overlaps on the GPU (e.g. on two streams without an
  *     ordering between them) race on it and give undefined results;
  *   - the first call on each device looks up the scratch array's device
- *     address (cudaGetSymbolAddress, with that device current); make that
- *     first call before any stream capture on the device.
+ *     address (cudaGetSymbolAddress, with that device current), and so does
+ *     the first call after the device's context has been re-created (e.g.
+ *     by cudaDeviceReset); make that first call before any stream capture
+ *     on the device.
  */
 #define WAN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 #define WAN_NOALLOC_MAX_ROW_HEADS (WAN_NOALLOC_SCRATCH_BYTES / 256u)

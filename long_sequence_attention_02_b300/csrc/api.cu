@@ -22,7 +22,9 @@ constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;  // 4 s per device-side wa
 struct DeviceState {
   bool probed = false;
   bool supported = false;
+  void* ctx = nullptr;  // the context the addresses below belong to
   int* err = nullptr;
+  void* noalloc = nullptr;  // device address of the allocation-free scratch (looked up on first use)
 };
 
 std::mutex g_mu;
@@ -49,12 +51,34 @@ int check_shapes(int B, long long L, int H, int head_dim) {
   return WAN_OK;
 }
 
+// The current CUDA context (driver entry point fetched through the runtime,
+// so the library needs no link-time dependency on libcuda). Device addresses
+// of the library's __device__ symbols belong to a context: after a
+// cudaDeviceReset (or any other re-creation of the primary context) the
+// module is loaded again and they may move, so they are cached per context.
+void* current_context() {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  static GetCurrentFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<GetCurrentFn>(p);
+  }
+  CUcontext c = nullptr;
+  if (fn == nullptr || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
 int device_state(DeviceState** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return WAN_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return WAN_ERR_UNSUPPORTED;
+  void* ctx = current_context();
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState& st = g_dev[dev];
+  if (st.probed && st.ctx != ctx) st = DeviceState();  // a new context: look the symbols up again
   if (!st.probed) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -66,6 +90,7 @@ int device_state(DeviceState** out) {
       if (cudaGetSymbolAddress(&p, g_wan_device_error) != cudaSuccess) return WAN_ERR_CUDA;
       st.err = static_cast<int*>(p);
     }
+    st.ctx = ctx;
     st.probed = true;
   }
   if (!st.supported) return WAN_ERR_UNSUPPORTED;
@@ -105,23 +130,20 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Scratch of wan_attn_fwd_noalloc: the rotated keys of one call. Held on
 // every device that loads the library; its device address is looked up once
-// per device (noalloc_scratch below), since in host code the name is only a
-// host-side stand-in.
+// per device and context (noalloc_scratch below), since in host code the
+// name is only a host-side stand-in.
 static __device__ __align__(256) uint8_t g_wan_noalloc_scratch[WAN_NOALLOC_SCRATCH_BYTES];
 
-void* g_noalloc_addr[kMaxDevices];  // device address of the scratch, per device (guarded by g_mu)
-
-int noalloc_scratch(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return WAN_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return WAN_ERR_UNSUPPORTED;
+// The scratch's device address for the current device and context (st from
+// device_state, which resets it when the context changes).
+int noalloc_scratch(DeviceState* st, void** out) {
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_noalloc_addr[dev] == nullptr) {
+  if (st->noalloc == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_wan_noalloc_scratch) != cudaSuccess || p == nullptr) return WAN_ERR_CUDA;
-    g_noalloc_addr[dev] = p;
+    st->noalloc = p;
   }
-  *out = g_noalloc_addr[dev];
+  *out = st->noalloc;
   return WAN_OK;
 }
 
@@ -362,7 +384,7 @@ int wan_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, f
   DeviceState* st = nullptr;
   if ((rc = device_state(&st)) != WAN_OK) return rc;
   void* scratch = nullptr;
-  if ((rc = noalloc_scratch(&scratch)) != WAN_OK) return rc;
+  if ((rc = noalloc_scratch(st, &scratch)) != WAN_OK) return rc;
   return wan_attn_fwd(q, k, v, o, lse, B, g, H, head_dim, tables, scale, scratch, WAN_NOALLOC_SCRATCH_BYTES,
                       stream);
 }

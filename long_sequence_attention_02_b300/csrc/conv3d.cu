@@ -24,6 +24,8 @@
 //
 // Warps: 0 TMA producer, 1 MMA issuer and TMEM owner, 2-5 epilogue
 // (TMEM -> + bias -> bf16 -> global, positions inside the picture only).
+// The CTAs are persistent (one per SM) and keep two accumulators in TMEM,
+// so that one tile's epilogue runs under the next tile's MMAs.
 // Every wait is bounded; on a timeout the device error word is set.
 #include <climits>
 
@@ -43,16 +45,41 @@ constexpr int kBTileMax = 256 * 128;          // up to 256 rows x 64 bf16
 constexpr int kStageC = kATile + kBTileMax;   // 48 KB
 constexpr int kConvSmem = kStagesC * kStageC + 1024;
 constexpr int kConvThreads = 192;
-constexpr uint32_t kConvTmemCols = 256;
 
 struct ConvArgs {
   const float* bias;     // [C_out] or null
   __nv_bfloat16* y;      // [B, T, H, W, C_out]
   int B, T, H, W, c_in, c_out, n_tile;
-  int tiles_h, tiles_w;
+  int tiles_h, tiles_w, tiles_n;
+  int n_tiles_total;     // B * tiles_h * tiles_w * T * tiles_n
+  uint32_t tmem_cols;    // power of two >= 2 * n_tile
   int has_cache;
   LaunchCommon lc;
 };
+
+// Output tile index -> (b, t, patch row, patch column, channel tile). The
+// channel tile runs fastest, then the frame, then the patch column: CTAs
+// that run at the same time work on neighbouring patches of all frames, so
+// the input windows they share (the two past frames of a tap, the halo of a
+// patch) are read from L2 rather than DRAM.
+struct ConvTile {
+  int b, t, h0, w0, n0;
+};
+__device__ __forceinline__ ConvTile conv_tile(int idx, const ConvArgs& a) {
+  ConvTile x;
+  const int nt = idx % a.tiles_n;
+  idx /= a.tiles_n;
+  x.t = idx % a.T;
+  idx /= a.T;
+  const int tw = idx % a.tiles_w;
+  idx /= a.tiles_w;
+  const int th = idx % a.tiles_h;
+  x.b = idx / a.tiles_h;
+  x.h0 = th * kPatchH;
+  x.w0 = tw * kPatchW;
+  x.n0 = nt * a.n_tile;
+  return x;
+}
 
 __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
                                             int c3, int c4) {
@@ -76,13 +103,18 @@ __device__ __forceinline__ void conv_abort(volatile int* abort, int* err) {
   atomicCAS(err, 0, kDevTimeout);
 }
 
+// Persistent: one CTA per SM walks the output tiles blockIdx.x,
+// blockIdx.x + gridDim.x, ... The ring of {A, B} stages runs on across
+// tiles, and TMEM holds two accumulators, so the epilogue of one tile
+// overlaps the MMAs of the next.
 __global__ void __launch_bounds__(kConvThreads, 1)
     causal_conv3d_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_cache,
                          const __grid_constant__ CUtensorMap tm_w, const ConvArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  __shared__ __align__(8) uint64_t bar_full[kStagesC], bar_empty[kStagesC], bar_acc;
+  __shared__ __align__(8) uint64_t bar_full[kStagesC], bar_empty[kStagesC];
+  __shared__ __align__(8) uint64_t bar_acc_full[2], bar_acc_empty[2], bar_drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -90,17 +122,6 @@ __global__ void __launch_bounds__(kConvThreads, 1)
   const int lane = threadIdx.x & 31;
   volatile int* abort = &abort_sh;
   const uint64_t to = a.lc.timeout_ns;
-
-  // Tile: (b, t, patch row, patch column) from blockIdx.x, channels from blockIdx.y.
-  int m = blockIdx.x;
-  const int tw = m % a.tiles_w;
-  m /= a.tiles_w;
-  const int th = m % a.tiles_h;
-  m /= a.tiles_h;
-  const int t = m % a.T;
-  const int b = m / a.T;
-  const int h0 = th * kPatchH, w0 = tw * kPatchW;
-  const int n0 = blockIdx.y * a.n_tile;
   const int c_steps = a.c_in / kChunkC;
   const int k_steps = 27 * c_steps;
 
@@ -109,12 +130,16 @@ __global__ void __launch_bounds__(kConvThreads, 1)
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
-    mbar_init(&bar_acc, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_acc_full[b], 1);
+      mbar_init(&bar_acc_empty[b], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(&bar_drain, 1);
     abort_sh = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base_sh, kConvTmemCols);
+    tmem_alloc(&tmem_base_sh, a.tmem_cols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -126,31 +151,36 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint32_t tx = static_cast<uint32_t>(kATile + a.n_tile * 128);
-      int k_end = 0;  // K steps walked (issued, or withheld by the test hook)
-      for (int k = 0; k < k_steps; ++k) {
-        const int slot = k % kStagesC;
-        if (k >= kStagesC && !mbar_wait(&bar_empty[slot], ((k / kStagesC) - 1) & 1, abort, to)) {
-          conv_abort(abort, a.lc.err);
-          break;
+      int g = 0;  // K steps walked over all of this CTA's tiles (issued, or withheld by the test hook)
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < a.n_tiles_total && ok; idx += gridDim.x) {
+        const ConvTile x = conv_tile(idx, a);
+        for (int k = 0; k < k_steps; ++k) {
+          const int slot = g % kStagesC;
+          if (g >= kStagesC && !mbar_wait(&bar_empty[slot], ((g / kStagesC) - 1) & 1, abort, to)) {
+            conv_abort(abort, a.lc.err);
+            ok = false;
+            break;
+          }
+          ++g;
+          if (a.lc.stall && g == 2) continue;  // test hook: the second K step never arrives
+          const int tap = k / c_steps;
+          const int c0 = (k % c_steps) * kChunkC;
+          const int kt = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
+          const int ti = x.t + kt - 2;  // input frame of this tap, < 0 before the chunk
+          uint8_t* sa = smem + slot * kStageC;
+          mbar_arrive_expect_tx(&bar_full[slot], tx);
+          if (ti < 0 && a.has_cache)
+            tma_load_5d(sa, &tm_cache, &bar_full[slot], c0, x.w0 + kw - 1, x.h0 + kh - 1, ti + 2, x.b);
+          else  // before a first chunk (ti < 0) the box lies outside x and reads zeros
+            tma_load_5d(sa, &tm_x, &bar_full[slot], c0, x.w0 + kw - 1, x.h0 + kh - 1, ti, x.b);
+          tma_load_3d(sa + kATile, &tm_w, &bar_full[slot], c0, tap, x.n0);
         }
-        k_end = k + 1;
-        if (a.lc.stall && k == 1) continue;  // test hook: K step 1 never arrives
-        const int tap = k / c_steps;
-        const int c0 = (k % c_steps) * kChunkC;
-        const int kt = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
-        const int ti = t + kt - 2;  // input frame of this tap, < 0 before the chunk
-        uint8_t* sa = smem + slot * kStageC;
-        mbar_arrive_expect_tx(&bar_full[slot], tx);
-        if (ti < 0 && a.has_cache)
-          tma_load_5d(sa, &tm_cache, &bar_full[slot], c0, w0 + kw - 1, h0 + kh - 1, ti + 2, b);
-        else  // before a first chunk (ti < 0) the box lies outside x and reads zeros
-          tma_load_5d(sa, &tm_x, &bar_full[slot], c0, w0 + kw - 1, h0 + kh - 1, ti, b);
-        tma_load_3d(sa + kATile, &tm_w, &bar_full[slot], c0, tap, n0);
       }
       // Every copy this warp issued lands before the CTA may exit (the last
       // fill of each slot is that barrier's latest phase; a withheld step's
       // wait just runs out).
-      for (int k = k_end - kStagesC < 0 ? 0 : k_end - kStagesC; k < k_end; ++k)
+      for (int k = g - kStagesC < 0 ? 0 : g - kStagesC; k < g; ++k)
         mbar_wait(&bar_full[k % kStagesC], (k / kStagesC) & 1, nullptr, to);
     }
     __syncwarp();
@@ -161,54 +191,82 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     const uint32_t hi = static_cast<uint32_t>(d0 >> 32);
     const uint32_t lo0 = static_cast<uint32_t>(d0);
     bool ok = true;
-    for (int k = 0; k < k_steps && ok; ++k) {
-      const int slot = k % kStagesC;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_full[slot], (k / kStagesC) & 1, abort, to));
-      if (!ok) {
-        if (lane == 0) conv_abort(abort, a.lc.err);
-        break;
+    int g = 0;  // K steps consumed
+    int i = 0;  // tiles of this CTA
+    for (int idx = blockIdx.x; idx < a.n_tiles_total && ok; idx += gridDim.x, ++i) {
+      const int ab = i & 1;
+      const uint32_t acc = tmem + static_cast<uint32_t>(ab * a.n_tile);
+      // The accumulator's previous tile has left TMEM.
+      if (i >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_empty[ab], ((i >> 1) - 1) & 1, abort, to));
+        if (!ok) {
+          if (lane == 0) conv_abort(abort, a.lc.err);
+          break;
+        }
+        tc_fence_after();
       }
-      tc_fence_after();
-      const uint32_t a_lo = lo0 + static_cast<uint32_t>(slot * (kStageC >> 4));
-      const uint32_t b_lo = a_lo + static_cast<uint32_t>(kATile >> 4);
+      for (int k = 0; k < k_steps; ++k, ++g) {
+        const int slot = g % kStagesC;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar_full[slot], (g / kStagesC) & 1, abort, to));
+        if (!ok) {
+          if (lane == 0) conv_abort(abort, a.lc.err);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_lo = lo0 + static_cast<uint32_t>(slot * (kStageC >> 4));
+        const uint32_t b_lo = a_lo + static_cast<uint32_t>(kATile >> 4);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)  // 16 channels (32 bytes) per MMA
-        umma_ss_elect_lo(tmem, a_lo + kk * 2, b_lo + kk * 2, hi, idesc, (k > 0 || kk > 0) ? 1u : 0u);
-      umma_commit_elect(&bar_empty[slot]);
+        for (int kk = 0; kk < 4; ++kk)  // 16 channels (32 bytes) per MMA
+          umma_ss_elect_lo(acc, a_lo + kk * 2, b_lo + kk * 2, hi, idesc, (k > 0 || kk > 0) ? 1u : 0u);
+        umma_commit_elect(&bar_empty[slot]);
+      }
+      if (ok) umma_commit_elect(&bar_acc_full[ab]);
     }
     // Also on the failure path: every issued MMA completes before TMEM is freed.
-    umma_commit_elect(&bar_acc);
-    mbar_wait(&bar_acc, 0, nullptr, to);
+    umma_commit_elect(&bar_drain);
+    mbar_wait(&bar_drain, 0, nullptr, to);
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31
     const int r = q * 32 + lane;
-    const int h = h0 + r / kPatchW, w = w0 + r % kPatchW;
-    const bool done = __all_sync(0xffffffffu, mbar_wait(&bar_acc, 0, abort, to));
-    if (!done && lane == 0) conv_abort(abort, a.lc.err);
-    if (done && !*abort) {
+    int i = 0;
+    for (int idx = blockIdx.x; idx < a.n_tiles_total; idx += gridDim.x, ++i) {
+      const int ab = i & 1;
+      const bool done = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full[ab], (i >> 1) & 1, abort, to));
+      if (!done || *abort) {
+        if (!done && lane == 0) conv_abort(abort, a.lc.err);
+        break;
+      }
       tc_fence_after();
+      const ConvTile x = conv_tile(idx, a);
+      const int h = x.h0 + r / kPatchW, w = x.w0 + r % kPatchW;
       const bool inside = h < a.H && w < a.W;
-      __nv_bfloat16* dst =
-          a.y + ((((size_t)b * a.T + t) * a.H + h) * a.W + w) * (size_t)a.c_out + n0;
+      __nv_bfloat16* dst = a.y + ((((size_t)x.b * a.T + x.t) * a.H + h) * a.W + w) * (size_t)a.c_out + x.n0;
+      const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ab * a.n_tile);
       for (int c = 0; c < a.n_tile / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c * 32), v);
+        tmem_ld32(acc + static_cast<uint32_t>(c * 32), v);
         tmem_ld_wait_regs(v);
+        if (c == a.n_tile / 32 - 1) {
+          // The accumulator may take the CTA's tile after next.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_acc_empty[ab]);
+        }
         if (inside) {
           uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float lo = __uint_as_float(v[2 * i]), hi2 = __uint_as_float(v[2 * i + 1]);
+          for (int k = 0; k < 16; ++k) {
+            float lo = __uint_as_float(v[2 * k]), hi2 = __uint_as_float(v[2 * k + 1]);
             if (a.bias) {
-              lo += a.bias[n0 + c * 32 + 2 * i];
-              hi2 += a.bias[n0 + c * 32 + 2 * i + 1];
+              lo += a.bias[x.n0 + c * 32 + 2 * k];
+              hi2 += a.bias[x.n0 + c * 32 + 2 * k + 1];
             }
-            pk[i] = pack_bf16x2(lo, hi2);
+            pk[k] = pack_bf16x2(lo, hi2);
           }
           uint4* o = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) o[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int k = 0; k < 4; ++k) o[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         }
       }
     }
@@ -218,7 +276,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kConvTmemCols);
+    tmem_dealloc(tmem, a.tmem_cols);
   }
 }
 
@@ -274,10 +332,19 @@ int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const
   a.n_tile = n_tile;
   a.tiles_h = (H + kPatchH - 1) / kPatchH;
   a.tiles_w = (W + kPatchW - 1) / kPatchW;
+  a.tiles_n = c_out / n_tile;
   a.has_cache = cache != nullptr;
   a.lc = lc;
-  const long long m_tiles = (long long)B * T * a.tiles_h * a.tiles_w;
-  if (m_tiles > INT_MAX || c_out / n_tile > 65535) return WAN_ERR_INVALID;
+  // Two accumulators of n_tile fp32 columns; TMEM is allocated in powers of two.
+  a.tmem_cols = 2 * n_tile <= 128 ? 128u : (2 * n_tile <= 256 ? 256u : 512u);
+  const long long total = (long long)B * T * a.tiles_h * a.tiles_w * a.tiles_n;
+  if (total > INT_MAX) return WAN_ERR_INVALID;
+  a.n_tiles_total = (int)total;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return WAN_ERR_CUDA;
+  const int grid = (int)(total < sms ? total : sms);  // persistent: one CTA per SM
 
   CUtensorMap tx, tc, tw;
   if (!make_tmap_act(&tx, x, B, T, H, W, c_in) ||
@@ -288,8 +355,7 @@ int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const
       cudaSuccess)
     return WAN_ERR_CUDA;
   record_start(lc, s);
-  causal_conv3d_kernel<<<dim3(static_cast<unsigned>(m_tiles), c_out / n_tile), kConvThreads, kConvSmem, s>>>(tx, tc,
-                                                                                                          tw, a);
+  causal_conv3d_kernel<<<grid, kConvThreads, kConvSmem, s>>>(tx, tc, tw, a);
   record_stop(lc, s);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }

@@ -84,3 +84,50 @@ def test_noalloc_rejects_problems_beyond_the_scratch():
     assert wan.wan_get_device_status() == wan.WAN_OK
     compare(dev_to_f64(o), dev_to_f64(o_ref), "O at the size limit")
     compare(dev_to_f64(lse), dev_to_f64(lse_ref), "LSE at the size limit")
+
+
+def test_noalloc_call_allocates_no_device_memory():
+    """After a first call (which loads the kernels and looks up the scratch's
+    address), a call on another problem leaves the device's free memory
+    unchanged: the entry point itself allocates nothing."""
+    grid_a, grid_b = (2, 8, 16), (3, 9, 10)
+    qa, ka, va = _inputs(1, grid_a, 2, 45)
+    qb, kb, vb = _inputs(1, grid_b, 3, 46)
+    ta, tb = wan.rope_tables(grid_a), wan.rope_tables(grid_b)
+    oa, lsea = torch.empty_like(qa), torch.empty(1, 2, 256, dtype=torch.float32, device="cuda")
+    ob, lseb = torch.empty_like(qb), torch.empty(1, 3, 270, dtype=torch.float32, device="cuda")
+    wan.check(wan.wan_attn_fwd_noalloc(qa, ka, va, oa, lsea, 1, grid_a, 2, 128, ta, 1 / math.sqrt(128)))
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    wan.check(wan.wan_attn_fwd_noalloc(qb, kb, vb, ob, lseb, 1, grid_b, 3, 128, tb, 1 / math.sqrt(128)))
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before, (free_before, free_after)
+    assert wan.wan_get_device_status() == wan.WAN_OK
+    o_ref, lse_ref = _with_workspace(qb, kb, vb, grid_b, tb)
+    compare(dev_to_f64(ob), dev_to_f64(o_ref), "O (no-allocation check)")
+
+
+def test_noalloc_on_a_side_stream_after_a_default_stream_call():
+    """The entry point runs on the caller's stream: a call on a non-default
+    stream, ordered after a call on the default stream that used the same
+    scratch, gives the workspace path's result."""
+    grid1, grid2 = (4, 8, 8), (2, 16, 16)
+    q1, k1, v1 = _inputs(1, grid1, 4, 47)
+    q2, k2, v2 = _inputs(2, grid2, 2, 48)
+    t1, t2 = wan.rope_tables(grid1), wan.rope_tables(grid2)
+    o1, lse1 = _without_workspace(q1, k1, v1, grid1, t1)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        o2 = torch.empty_like(q2)
+        lse2 = torch.empty(2, 2, 512, dtype=torch.float32, device="cuda")
+        wan.check(wan.wan_attn_fwd_noalloc(q2, k2, v2, o2, lse2, 2, grid2, 2, 128, t2, 1 / math.sqrt(128), side),
+                  "wan_attn_fwd_noalloc (side stream)")
+    side.synchronize()
+    assert wan.wan_get_device_status() == wan.WAN_OK
+    o1_ref, lse1_ref = _with_workspace(q1, k1, v1, grid1, t1)
+    o2_ref, lse2_ref = _with_workspace(q2, k2, v2, grid2, t2)
+    compare(dev_to_f64(o1), dev_to_f64(o1_ref), "O (default stream)")
+    compare(dev_to_f64(o2), dev_to_f64(o2_ref), "O (side stream)")
+    compare(dev_to_f64(lse2), dev_to_f64(lse2_ref), "LSE (side stream)")
