@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 
-ATTN_SOURCES = ["api.cu", "rope.cu", "attn_fwd.cu", "attn_fwd_fp8.cu", "attn_bwd.cu", "conv3d.cu"]
+ATTN_SOURCES = ["api.cu", "rope.cu", "rows.cu", "attn_fwd.cu", "attn_fwd_fp8.cu", "attn_bwd.cu", "conv3d.cu"]
 ATTN_HEADERS = ["common.cuh", "kernels.cuh"]
 ATTN_LIB = os.path.join(HERE, "libwan_attn.so")
 SYNTH_LIB = os.path.join(HERE, "libwan_synth.so")

@@ -547,64 +547,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// D_i = sum_d dO_id O_id and LSE_i * log2(e) into rows padded to a multiple
-// of 128 (pad: D = 0, LSE = +inf). A block of 128 threads walks tokens (all H
-// heads of one (b, l) per step, H * 256 contiguous bytes of O and of dO);
-// thread (c, g) = (tid % 16, tid / 16) reads the 16-byte chunk c of heads
-// g, g + 8, ..., so the 16 lanes c of one head reduce its dot product with
-// shuffles and lane c = 0 writes the row's two floats.
-__global__ void __launch_bounds__(128) bwd_rows_kernel(const uint4* o, const uint4* dout, const float* lse,
-                                                       float* lse2, float* drow, long long n_tokens, int L, int Lpad,
-                                                       int H) {
-  constexpr int kHeadsPerPass = 4;
-  const int c = threadIdx.x & 15;
-  const int g = threadIdx.x >> 4;
-  const unsigned group = 0xFFFFu << (threadIdx.x & 16);  // the 16 lanes of one head
-  for (long long tok = blockIdx.x; tok < n_tokens; tok += gridDim.x) {
-    const int l = static_cast<int>(tok % L);
-    const long long b = tok / L;
-    const size_t tok_chunk = static_cast<size_t>(tok) * H * 16 + c;
-    for (int h0 = g; h0 < H; h0 += 8 * kHeadsPerPass) {
-      uint4 xo[kHeadsPerPass], yo[kHeadsPerPass];
-#pragma unroll
-      for (int u = 0; u < kHeadsPerPass; ++u)
-        if (h0 + 8 * u < H) {
-          const size_t i = tok_chunk + static_cast<size_t>(h0 + 8 * u) * 16;
-          xo[u] = o[i];
-          yo[u] = dout[i];
-        }
-#pragma unroll
-      for (int u = 0; u < kHeadsPerPass; ++u) {
-        const int h = h0 + 8 * u;
-        if (h >= H) break;
-        const uint32_t xa[4] = {xo[u].x, xo[u].y, xo[u].z, xo[u].w}, ya[4] = {yo[u].x, yo[u].y, yo[u].z, yo[u].w};
-        float acc = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          acc = fmaf(__uint_as_float(xa[k] << 16), __uint_as_float(ya[k] << 16), acc);
-          acc = fmaf(__uint_as_float(xa[k] & 0xFFFF0000u), __uint_as_float(ya[k] & 0xFFFF0000u), acc);
-        }
-#pragma unroll
-        for (int m = 8; m >= 1; m >>= 1) acc += __shfl_xor_sync(group, acc, m, 16);
-        if (c == 0) {
-          const size_t bh = static_cast<size_t>(b) * H + h;
-          drow[bh * Lpad + l] = acc;
-          lse2[bh * Lpad + l] = lse[bh * L + l] * 1.4426950408889634f;
-        }
-      }
-    }
-  }
-}
-
-__global__ void bwd_pad_kernel(float* lse2, float* drow, int BH, int L, int Lpad) {
-  const int pad = Lpad - L;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < BH * pad; i += gridDim.x * blockDim.x) {
-    const size_t dst = (size_t)(i / pad) * Lpad + L + (i % pad);
-    lse2[dst] = INFINITY;
-    drow[dst] = 0.f;
-  }
-}
-
 size_t align_up(size_t x) { return (x + 255) / 256 * 256; }
 
 struct BwdWorkspace {
@@ -658,11 +600,8 @@ int launch_attn_bwd(const void* q, const void* k, const void* v, const void* o, 
   const long long n_rows = (long long)B * L * H;
   {
     record_pass(lc, kPassRows, 0, s);
-    const long long n_tokens = (long long)B * L, cap = (long long)sms * 16;  // 16 blocks of 128 threads per SM
-    bwd_rows_kernel<<<(int)(n_tokens < cap ? n_tokens : cap), 128, 0, s>>>(
-        (const uint4*)o, (const uint4*)dout, lse, w.lse2, w.drow, n_tokens, L, Lpad, H);
+    if (launch_bwd_rows(o, dout, lse, w.lse2, w.drow, B, L, Lpad, H, s) != cudaSuccess) return WAN_ERR_CUDA;
     record_pass(lc, kPassRows, 1, s);
-    if (Lpad > L) bwd_pad_kernel<<<sms, 256, 0, s>>>(w.lse2, w.drow, B * H, L, Lpad);
   }
   if (cudaMemsetAsync(w.dq_acc, 0, (size_t)n_rows * 512, s) != cudaSuccess) return WAN_ERR_CUDA;
 

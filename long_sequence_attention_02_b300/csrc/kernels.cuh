@@ -55,6 +55,12 @@ cudaError_t launch_rope_rotate_bf16_rows(const void* x, void* y, int B, int L, i
 cudaError_t launch_rope_unrotate_f32(const float* x, void* y, int B, wan_grid_t g, int H, RopeTables tab,
                                      cudaStream_t s);
 
+// Backward row pass: D = rowsum(dO * O) and LSE * log2(e) into [B*H][Lpad]
+// rows (pad: D = 0, LSE = +inf), for bf16 O, dO [B, L, H, 128] and fp32 LSE
+// [B, H, L].
+cudaError_t launch_bwd_rows(const void* o, const void* dout, const float* lse, float* lse2, float* drow, int B, int L,
+                            int Lpad, int H, cudaStream_t s);
+
 // How the forward epilogue combines this call's result with what o / lse hold.
 enum FwdMerge : int {
   kMergeNone = 0,  // o, lse <- this call's attention
