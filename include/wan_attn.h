@@ -294,8 +294,10 @@ int wan_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, f
  *               (cache or zeros) ++ x for the next chunk; may be NULL, and may
  *               be the same buffer as cache (it is written after the
  *               convolution has read cache, in stream order)
- * c_in and c_out must be multiples of 64 (WAN_ERR_UNSUPPORTED otherwise);
- * bf16 pointers 16-byte aligned, bias 4-byte aligned. B = 0 is a no-op.
+ * c_in and c_out must be multiples of 32 (WAN_ERR_UNSUPPORTED otherwise; a
+ * C_in that is not a multiple of 64, such as the 96 channels of the VAE's
+ * outer stages, is reduced in 32-channel steps); bf16 pointers 16-byte
+ * aligned, bias 4-byte aligned. B = 0 is a no-op.
  * The reduction is accumulated in fp32 on tensor cores; y is rounded to bf16.
  */
 int wan_vae_causal_conv3d(const void* x, const void* cache, const void* weight, const float* bias, void* y,

@@ -394,7 +394,7 @@ int wan_vae_causal_conv3d(const void* x, const void* cache, const void* weight, 
   if (B < 0 || T <= 0 || H <= 0 || W <= 0 || c_in <= 0 || c_out <= 0 || B > 65535 || T > 65535 || H > 65535 ||
       W > 65535)
     return WAN_ERR_INVALID;
-  if (c_in % 64 != 0 || c_in > 8192 || c_out > 8192 || wan::conv3d_n_tile(c_out) == 0) return WAN_ERR_UNSUPPORTED;
+  if (c_in % 32 != 0 || c_in > 8192 || c_out > 8192 || wan::conv3d_n_tile(c_out) == 0) return WAN_ERR_UNSUPPORTED;
   if (B == 0) return WAN_OK;
   if (!x || !weight || !y) return WAN_ERR_INVALID;
   if (!aligned16(x) || !aligned16(weight) || !aligned16(y) || (cache && !aligned16(cache)) ||

@@ -11,16 +11,17 @@
 //
 // GEMM view: M = output positions, N = C_out, K = 27 taps x C_in. One CTA
 // computes a tile of 128 positions x N channels: the positions are an 8 (h)
-// x 16 (w) patch of one frame, N the largest of 256, 192, 128 and 64 that
-// divides C_out. Per K step (one tap, 64 input channels):
-// - A = the 128 input pixels that tap reads, 64 channels each: one 5D TMA box
-//   {64 c, 16 w, 8 h, 1 t, 1 b} at the tap's offset. Its zero fill outside
+// x 16 (w) patch of one frame, N = C_out when C_out <= 256, else the largest
+// of 256, 192, 128, 64 and 32 that divides C_out. Per K step (one tap, kc =
+// 64 input channels, or 32 when C_in is not a multiple of 64):
+// - A = the 128 input pixels that tap reads, kc channels each: one 5D TMA box
+//   {kc c, 16 w, 8 h, 1 t, 1 b} at the tap's offset. Its zero fill outside
 //   the tensor is the spatial padding, and, for a first chunk, the causal
 //   padding too (a negative frame coordinate). With a cache, taps that reach
 //   before the chunk read the cache tensor instead.
-// - B = the tap's N x 64 weights: one 3D box {64 c, 1 tap, N}.
-// Both land 128B-swizzled (rows of 128 bytes), and four tcgen05.mma of
-// kind::f16 (K = 16 each) accumulate into TMEM.
+// - B = the tap's N x kc weights: one 3D box {kc c, 1 tap, N}.
+// Both land swizzled (rows of 2 kc bytes, 128- or 64-byte swizzle), and kc/16
+// tcgen05.mma of kind::f16 (K = 16 each) accumulate into TMEM.
 //
 // Warps: 0 TMA producer, 1 MMA issuer and TMEM owner, 2-5 epilogue
 // (TMEM -> + bias -> bf16 -> global, positions inside the picture only).
@@ -38,13 +39,22 @@ namespace {
 
 constexpr int kPatchH = 8;
 constexpr int kPatchW = 16;                   // 128 output positions per tile
-constexpr int kChunkC = 64;                   // input channels per K step (128 bytes)
-constexpr int kStagesC = 4;
-constexpr int kATile = 128 * 128;             // 128 rows x 64 bf16
-constexpr int kBTileMax = 256 * 128;          // up to 256 rows x 64 bf16
-constexpr int kStageC = kATile + kBTileMax;   // 48 KB
-constexpr int kConvSmem = kStagesC * kStageC + 1024;
 constexpr int kConvThreads = 192;
+constexpr int kRingBytes = 192 * 1024;        // the {A, B} stage ring
+
+// One K step covers kC input channels of one tap: 64 (rows of 128 bytes,
+// 128-byte swizzle) when C_in is a multiple of 64, else 32 (rows of 64 bytes,
+// 64-byte swizzle) for layers such as the VAE's 96-channel ones.
+template <int kC>
+struct ConvCfg {
+  static constexpr int kRow = kC * 2;                  // bytes per row of A and B
+  static constexpr int kATile = 128 * kRow;            // 128 input pixels
+  static constexpr int kBTileMax = 256 * kRow;         // up to 256 output channels
+  static constexpr int kStage = kATile + kBTileMax;    // 48 KB / 24 KB
+  static constexpr int kStages = kRingBytes / kStage;  // 4 / 8
+  static constexpr int kSmem = kStages * kStage + 1024;
+  static constexpr uint32_t kSwizzle = kC == 64 ? 2u : 4u;  // descriptor layout: SWIZZLE_128B / SWIZZLE_64B
+};
 
 struct ConvArgs {
   const float* bias;     // [C_out] or null
@@ -103,13 +113,29 @@ __device__ __forceinline__ void conv_abort(volatile int* abort, int* err) {
   atomicCAS(err, 0, kDevTimeout);
 }
 
+// Shared-memory matrix descriptor of a K-major tile with rows of kRow bytes
+// in the swizzle matching the TMA box: bits [0,14) start >> 4, [16,30) LBO >> 4
+// (unused for these K-major swizzled tiles), [32,46) SBO >> 4 (8 rows),
+// [46,48) = 1 (tcgen05 descriptor version), [61,64) swizzle mode.
+template <int kC>
+__device__ __forceinline__ uint64_t conv_desc(uint32_t saddr) {
+  constexpr uint32_t kSbo = 8 * ConvCfg<kC>::kRow;
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(kSbo >> 4) << 32) | (1ull << 46) |
+         ((uint64_t)ConvCfg<kC>::kSwizzle << 61);
+}
+
 // Persistent: one CTA per SM walks the output tiles blockIdx.x,
 // blockIdx.x + gridDim.x, ... The ring of {A, B} stages runs on across
 // tiles, and TMEM holds two accumulators, so the epilogue of one tile
 // overlaps the MMAs of the next.
+template <int kC>
 __global__ void __launch_bounds__(kConvThreads, 1)
     causal_conv3d_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_cache,
                          const __grid_constant__ CUtensorMap tm_w, const ConvArgs a) {
+  using Cfg = ConvCfg<kC>;
+  constexpr int kStagesC = Cfg::kStages;
+  constexpr int kATile = Cfg::kATile;
+  constexpr int kStageC = Cfg::kStage;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -122,7 +148,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
   const int lane = threadIdx.x & 31;
   volatile int* abort = &abort_sh;
   const uint64_t to = a.lc.timeout_ns;
-  const int c_steps = a.c_in / kChunkC;
+  const int c_steps = a.c_in / kC;
   const int k_steps = 27 * c_steps;
 
   if (threadIdx.x == 0) {
@@ -150,7 +176,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint32_t tx = static_cast<uint32_t>(kATile + a.n_tile * 128);
+      const uint32_t tx = static_cast<uint32_t>(kATile + a.n_tile * Cfg::kRow);
       int g = 0;  // K steps walked over all of this CTA's tiles (issued, or withheld by the test hook)
       bool ok = true;
       for (int idx = blockIdx.x; idx < a.n_tiles_total && ok; idx += gridDim.x) {
@@ -165,7 +191,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
           ++g;
           if (a.lc.stall && g == 2) continue;  // test hook: the second K step never arrives
           const int tap = k / c_steps;
-          const int c0 = (k % c_steps) * kChunkC;
+          const int c0 = (k % c_steps) * kC;
           const int kt = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
           const int ti = x.t + kt - 2;  // input frame of this tap, < 0 before the chunk
           uint8_t* sa = smem + slot * kStageC;
@@ -187,7 +213,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(a.n_tile), 0, 0);
-    const uint64_t d0 = sdesc_sw128(smem_u32(smem), 16, 1024);
+    const uint64_t d0 = conv_desc<kC>(smem_u32(smem));
     const uint32_t hi = static_cast<uint32_t>(d0 >> 32);
     const uint32_t lo0 = static_cast<uint32_t>(d0);
     bool ok = true;
@@ -216,7 +242,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         const uint32_t a_lo = lo0 + static_cast<uint32_t>(slot * (kStageC >> 4));
         const uint32_t b_lo = a_lo + static_cast<uint32_t>(kATile >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // 16 channels (32 bytes) per MMA
+        for (int kk = 0; kk < kC / 16; ++kk)  // 16 channels (32 bytes) per MMA
           umma_ss_elect_lo(acc, a_lo + kk * 2, b_lo + kk * 2, hi, idesc, (k > 0 || kk > 0) ? 1u : 0u);
         umma_commit_elect(&bar_empty[slot]);
       }
@@ -281,37 +307,40 @@ __global__ void __launch_bounds__(kConvThreads, 1)
 }
 
 // bf16 channels-last activations [B, frames, H, W, C] -> 5D tiled map, box
-// {64 c, 16 w, 8 h, 1, 1}, 128-byte swizzle, zero fill outside.
-bool make_tmap_act(CUtensorMap* map, const void* base, int B, int frames, int H, int W, int C) {
+// {kc c, 16 w, 8 h, 1, 1}, 128-byte (kc = 64) or 64-byte (kc = 32) swizzle,
+// zero fill outside.
+bool make_tmap_act(CUtensorMap* map, const void* base, int B, int frames, int H, int W, int C, int kc) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   const cuuint64_t c2 = (cuuint64_t)C * 2;
   cuuint64_t dims[5] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)frames, (cuuint64_t)B};
   cuuint64_t strides[4] = {c2, c2 * W, c2 * W * H, c2 * W * H * frames};
-  cuuint32_t box[5] = {kChunkC, kPatchW, kPatchH, 1, 1};
+  cuuint32_t box[5] = {(cuuint32_t)kc, kPatchW, kPatchH, 1, 1};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, kc == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Weights [C_out, 27, C_in] -> 3D tiled map, box {64 c, 1 tap, n_tile rows}.
-bool make_tmap_wt(CUtensorMap* map, const void* base, int c_in, int c_out, int n_tile) {
+// Weights [C_out, 27, C_in] -> 3D tiled map, box {kc c, 1 tap, n_tile rows}.
+bool make_tmap_wt(CUtensorMap* map, const void* base, int c_in, int c_out, int n_tile, int kc) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)c_in, 27, (cuuint64_t)c_out};
   cuuint64_t strides[2] = {(cuuint64_t)c_in * 2, (cuuint64_t)c_in * 2 * 27};
-  cuuint32_t box[3] = {kChunkC, 1, (cuuint32_t)n_tile};
+  cuuint32_t box[3] = {(cuuint32_t)kc, 1, (cuuint32_t)n_tile};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, kc == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
 int conv3d_n_tile(int c_out) {
-  for (int n : {256, 192, 128, 64})
+  if (c_out % 32 != 0) return 0;
+  if (c_out <= 256) return c_out;  // one channel tile (an MMA N is any multiple of 16 up to 256)
+  for (int n : {256, 192, 128, 64, 32})
     if (c_out % n == 0) return n;
   return 0;
 }
@@ -319,7 +348,8 @@ int conv3d_n_tile(int c_out) {
 int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const float* bias, void* y, int B, int T,
                          int H, int W, int c_in, int c_out, const LaunchCommon& lc, cudaStream_t s) {
   const int n_tile = conv3d_n_tile(c_out);
-  if (n_tile == 0 || c_in % kChunkC != 0) return WAN_ERR_UNSUPPORTED;
+  if (n_tile == 0 || c_in % 32 != 0) return WAN_ERR_UNSUPPORTED;
+  const int kc = c_in % 64 == 0 ? 64 : 32;  // input channels per K step
   ConvArgs a;
   a.bias = bias;
   a.y = static_cast<__nv_bfloat16*>(y);
@@ -347,15 +377,16 @@ int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const
   const int grid = (int)(total < sms ? total : sms);  // persistent: one CTA per SM
 
   CUtensorMap tx, tc, tw;
-  if (!make_tmap_act(&tx, x, B, T, H, W, c_in) ||
-      !make_tmap_act(&tc, cache ? cache : x, B, cache ? 2 : T, H, W, c_in) ||
-      !make_tmap_wt(&tw, wt, c_in, c_out, n_tile))
+  if (!make_tmap_act(&tx, x, B, T, H, W, c_in, kc) ||
+      !make_tmap_act(&tc, cache ? cache : x, B, cache ? 2 : T, H, W, c_in, kc) ||
+      !make_tmap_wt(&tw, wt, c_in, c_out, n_tile, kc))
     return WAN_ERR_CUDA;
-  if (cudaFuncSetAttribute(causal_conv3d_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kConvSmem) !=
-      cudaSuccess)
+  auto kern = kc == 64 ? causal_conv3d_kernel<64> : causal_conv3d_kernel<32>;
+  const int smem = kc == 64 ? ConvCfg<64>::kSmem : ConvCfg<32>::kSmem;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return WAN_ERR_CUDA;
   record_start(lc, s);
-  causal_conv3d_kernel<<<grid, kConvThreads, kConvSmem, s>>>(tx, tc, tw, a);
+  kern<<<grid, kConvThreads, smem, s>>>(tx, tc, tw, a);
   record_stop(lc, s);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }

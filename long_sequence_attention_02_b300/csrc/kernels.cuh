@@ -89,7 +89,7 @@ int launch_attn_bwd(const void* q, const void* k, const void* v, const void* o, 
                     void* workspace, const LaunchCommon& lc, cudaStream_t s);
 
 // Causal 3 x 3 x 3 Conv3d of the Wan-VAE on one chunk (conv3d.cu). cache may
-// be null (zeros before the chunk). c_in % 64 == 0; conv3d_n_tile(c_out) > 0.
+// be null (zeros before the chunk). c_in % 32 == 0; conv3d_n_tile(c_out) > 0.
 int conv3d_n_tile(int c_out);
 int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const float* bias, void* y, int B, int T,
                          int H, int W, int c_in, int c_out, const LaunchCommon& lc, cudaStream_t s);

@@ -93,4 +93,6 @@ CONV_WORKLOADS = {
     "wan_vae_conv3d_720p_384": ConvWorkload("wan_vae_conv3d_720p_384", 1, 4, 90, 160, 384, 384),
     # 4 frames of 360 x 640 (720p / 2), 192 -> 192: 354 MB of input, > L2; the timed layer
     "wan_vae_conv3d_360x640_192": ConvWorkload("wan_vae_conv3d_360x640_192", 1, 4, 360, 640, 192, 192),
+    # 4 frames of 720 x 1280 (full 720p), 96 -> 96: an outer stage, reduced in 32-channel K steps
+    "wan_vae_conv3d_720x1280_96": ConvWorkload("wan_vae_conv3d_720x1280_96", 1, 4, 720, 1280, 96, 96),
 }

@@ -218,8 +218,9 @@ def test_conv3d_rejects_bad_arguments(lib):
     assert call(bias=FAKE + 2) == wan.WAN_ERR_INVALID
     assert call(T=0) == wan.WAN_ERR_INVALID
     assert call(H=-1) == wan.WAN_ERR_INVALID
-    assert call(c_in=96) == wan.WAN_ERR_UNSUPPORTED         # channels must be multiples of 64
-    assert call(c_out=32) == wan.WAN_ERR_UNSUPPORTED
+    assert call(c_in=80) == wan.WAN_ERR_UNSUPPORTED         # channels must be multiples of 32
+    assert call(c_out=48) == wan.WAN_ERR_UNSUPPORTED
+    assert call(c_out=8224) == wan.WAN_ERR_UNSUPPORTED       # more than 8192 output channels
     assert call(y=X + frame) == wan.WAN_ERR_INVALID          # output overlapping the input
     assert call(cache_out=X) == wan.WAN_ERR_INVALID          # next cache over the input
     assert call(cache_out=C + 64) == wan.WAN_ERR_INVALID     # partly over the cache it reads

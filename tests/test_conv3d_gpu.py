@@ -47,6 +47,10 @@ def _run(x, cache, wt, bias, cache_out=True, stream=None):
     (1, 1, 8, 16, 128, 192, False, True),    # first chunk of one frame, N = 192
     (1, 2, 5, 33, 64, 256, True, False),     # N = 256, no bias
     (1, 4, 9, 17, 128, 320, False, True),    # N = 64 (320 = 5 x 64)
+    (1, 2, 9, 17, 96, 96, True, True),       # 32-channel K steps (C_in 96), N = 96
+    (1, 3, 8, 16, 32, 64, False, True),      # C_in 32: one K step per tap
+    (2, 1, 5, 33, 160, 224, True, False),    # C_in 160 = 5 x 32, N = 224
+    (1, 2, 7, 18, 96, 320, True, True),      # 32-channel K steps, N = 64 x 5
 ])
 def test_conv3d_every_output(B, T, H, W, c_in, c_out, with_cache, with_bias):
     x, cache, wt, bias = _layer(21, B, T, H, W, c_in, c_out, with_cache, with_bias)
@@ -129,4 +133,40 @@ def test_conv3d_timed_layer_sampled():
     got = dev_to_f64(torch.stack([y[p] for p in pos]))
     ref = vae.causal_conv3d_at(f64(x), f64(wt), bias.astype(np.float64), f64(cache), pos)
     compare(got, ref, "y (timed layer, sampled)")
+    assert np.array_equal(dev_to_f64(co), f64(x[:, -2:])), "next cache"
+
+
+def test_conv3d_96_channels_chunks_equal_the_whole_video():
+    """The 32-channel K-step path through the cache: chunks of 1, 4 and 4 frames
+    are bit for bit the whole-sequence call, and match the oracle."""
+    B, T, H, W, c_in, c_out = 1, 9, 8, 20, 96, 96
+    x, _, wt, bias = _layer(28, B, T, H, W, c_in, c_out, False, True)
+    xd = to_dev(x)
+    whole, _ = _run(xd, None, wt, bias)
+    outs, cache, t0 = [], None, 0
+    for n in (1, 4, 4):
+        y, cache = _run(xd[:, t0:t0 + n].contiguous(), cache, wt, bias)
+        outs.append(y)
+        t0 += n
+    assert torch.equal(torch.cat(outs, dim=1), whole)
+    y_ref, _ = vae.causal_conv3d(f64(x), f64(wt), bias.astype(np.float64))
+    compare(dev_to_f64(whole), y_ref, "96-channel y")
+
+
+def test_conv3d_96_channel_720p_layer_sampled():
+    """A full-resolution 720p outer-stage layer (4 frames of 720 x 1280, 96 -> 96
+    channels, with a cache) on 512 seeded positions plus corners and edges."""
+    from long_sequence_attention_02_b300.workloads import CONV_WORKLOADS
+
+    w = CONV_WORKLOADS["wan_vae_conv3d_720x1280_96"]
+    x, cache, wt, bias = _layer(29, w.B, w.T, w.H, w.W, w.c_in, w.c_out, True, True)
+    y, co = _run(x, cache, wt, bias)
+    rng = np.random.default_rng(30)
+    n = 512
+    T, H, W = w.T, w.H, w.W
+    pos = [(0, 0, 0, 0), (0, T - 1, H - 1, W - 1), (0, 0, H - 1, 0), (0, T - 1, 0, W - 1), (0, 1, H - 8, W - 16)]
+    pos += list(zip(rng.integers(0, w.B, n), rng.integers(0, T, n), rng.integers(0, H, n), rng.integers(0, W, n)))
+    got = dev_to_f64(torch.stack([y[p] for p in pos]))
+    ref = vae.causal_conv3d_at(f64(x), f64(wt), bias.astype(np.float64), f64(cache), pos)
+    compare(got, ref, "y (96-channel 720p layer, sampled)")
     assert np.array_equal(dev_to_f64(co), f64(x[:, -2:])), "next cache"
