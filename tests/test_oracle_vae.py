@@ -158,3 +158,77 @@ def test_sampled_positions_match_the_layer():
 
 def test_flop_count():
     assert vae.conv3d_flops(1, 4, 90, 160, 384, 384) == 2 * 4 * 90 * 160 * 384 * 27 * 384
+
+
+# ---------------------------------------------------------------------------
+# Time-downsampling layer (stride 2 in time, one cached frame)
+
+
+def _brute_down(x, wt, bias, cache):
+    """Loops over (b, j, h, w, o) and the three taps: output frame j reads
+    frames 2j - 1, 2j and 2j + 1 of the chunk, frame -1 being the cache."""
+    B, T, H, W, Ci = x.shape
+    Co = wt.shape[0]
+    y = np.zeros((B, T // 2, H, W, Co))
+    for b in range(B):
+        for j in range(T // 2):
+            for h in range(H):
+                for w in range(W):
+                    for o in range(Co):
+                        s = bias[o]
+                        for kt in range(3):
+                            ti = 2 * j + kt - 1
+                            src = x[b, ti, h, w] if ti >= 0 else cache[b, 0, h, w]
+                            for c in range(Ci):
+                                s += wt[o, kt, c] * src[c]
+                        y[b, j, h, w, o] = s
+    return y
+
+
+def test_time_downsample_matches_brute_force():
+    rng = np.random.default_rng(61)
+    x, cache = _rand(rng, 2, 4, 3, 2, 5), _rand(rng, 2, 1, 3, 2, 5)
+    wt, bias = _rand(rng, 4, 3, 5), _rand(rng, 4)
+    y, new_cache = vae.causal_time_downsample(x, wt, bias, cache)
+    np.testing.assert_allclose(y, _brute_down(x, wt, bias, cache), atol=1e-12)
+    assert y.shape[1] == 2                              # exactly half the frames
+    np.testing.assert_array_equal(new_cache, x[:, -1:])
+
+
+def test_time_downsample_first_chunk_passes_through():
+    rng = np.random.default_rng(62)
+    x = _rand(rng, 1, 1, 4, 3, 6)
+    y, new_cache = vae.causal_time_downsample(x, _rand(rng, 6, 3, 6), _rand(rng, 6), None)
+    np.testing.assert_array_equal(y, x)
+    np.testing.assert_array_equal(new_cache, x)
+
+
+def test_time_downsample_one_hot_taps_select_frames():
+    rng = np.random.default_rng(63)
+    x, cache = _rand(rng, 1, 6, 2, 2, 3), _rand(rng, 1, 1, 2, 2, 3)
+    for kt, shift in ((0, -1), (1, 0), (2, 1)):
+        wt = np.zeros((3, 3, 3))
+        wt[:, kt, :] = np.eye(3)
+        y, _ = vae.causal_time_downsample(x, wt, None, cache)
+        for j in range(3):
+            src = x[:, 2 * j + shift] if 2 * j + shift >= 0 else cache[:, 0]
+            np.testing.assert_array_equal(y[:, j], src)
+
+
+def test_time_downsample_chunks_equal_the_whole_sequence():
+    """Chunks of 1, 4, 4 frames through the one-frame cache give the
+    whole-sequence definition: frame 0 unchanged, then output j >= 1 reads
+    frames 2j - 2, 2j - 1 and 2j of the video."""
+    rng = np.random.default_rng(64)
+    T = 9
+    x = _rand(rng, 1, T, 3, 4, 5)
+    wt, bias = _rand(rng, 5, 3, 5), _rand(rng, 5)
+    got = vae.causal_time_downsample_chunked(x, wt, bias)
+    assert got.shape[1] == 1 + (T - 1) // 2
+    want = np.zeros_like(got)
+    want[:, 0] = x[:, 0]
+    for j in range(1, got.shape[1]):
+        want[:, j] = bias + sum(np.einsum("bhwc,oc->bhwo", x[:, 2 * j - 2 + kt], wt[:, kt]) for kt in range(3))
+    np.testing.assert_allclose(got, want, atol=1e-12)
+    other = vae.causal_time_downsample_chunked(x, wt, bias, chunks=[1, 2, 6])
+    np.testing.assert_allclose(other, want, atol=1e-12)
