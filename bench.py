@@ -34,6 +34,7 @@ sys.path.insert(0, HERE)
 METRIC = "attention TFLOP/s (bf16 fwd/bwd) at 32,760 and 75,600 tokens; % of dense BF16 peak"
 # Lines for the VAE layer (--workload wan_vae_conv3d_*), a secondary workload.
 CONV_METRIC = "causal Conv3d TFLOP/s (bf16, 2 FLOP per multiply-add); % of dense BF16 peak"
+CONV_KINDS = ("conv3d", "time_down")
 L2_BYTES = 126 * 2 ** 20
 
 
@@ -185,22 +186,26 @@ class Case:
 
 
 def make_conv_case(wan, torch, dev, w, rank, seed=0):
-    """One causal Conv3d layer of the VAE on a chunk with its 2-frame cache."""
+    """One causal Conv3d layer of the VAE on a chunk with its 2-frame cache, or
+    (kind "time_down") one time-downsampling layer with its 1-frame cache."""
     B, T, H, W, ci, co = w.B, w.T, w.H, w.W, w.c_in, w.c_out
+    down = w.kind == "time_down"
     gen = torch.Generator(device=dev)
     gen.manual_seed(input_seed(seed, rank))
     stream = torch.cuda.current_stream(dev)
     c = Case()
     c.stream = stream
     x = torch.randn(B, T, H, W, ci, device=dev, generator=gen).bfloat16()
-    cache = torch.randn(B, 2, H, W, ci, device=dev, generator=gen).bfloat16()
-    wt = (torch.randn(co, 3, 3, 3, ci, device=dev, generator=gen) / math.sqrt(27 * ci)).bfloat16()
+    cache = torch.randn(B, 1 if down else 2, H, W, ci, device=dev, generator=gen).bfloat16()
+    taps = (3,) if down else (3, 3, 3)
+    wt = (torch.randn(co, *taps, ci, device=dev, generator=gen) / math.sqrt(w.taps() * ci)).bfloat16()
     bias = torch.randn(co, device=dev, generator=gen) * 0.1
-    y = torch.empty(B, T, H, W, co, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(B, w.t_out(), H, W, co, dtype=torch.bfloat16, device=dev)
     cache_out = torch.empty_like(cache)
+    entry = wan.wan_vae_time_downsample if down else wan.wan_vae_causal_conv3d
 
     def run():
-        wan.check(wan.wan_vae_causal_conv3d(x, cache, wt, bias, y, cache_out, B, T, H, W, ci, co, stream))
+        wan.check(entry(x, cache, wt, bias, y, cache_out, B, T, H, W, ci, co, stream))
 
     c.inputs, c.outputs = [x, cache, wt, bias], [y, cache_out]
     c.flops = c.kernel_flops = w.flops()
@@ -223,7 +228,7 @@ def input_seed(seed: int, rank: int) -> int:
 
 
 def make_case(wan, torch, dev, w, rank, peaks, seed=0):
-    if w.kind == "conv3d":
+    if w.kind in CONV_KINDS:
         return make_conv_case(wan, torch, dev, w, rank, seed)
     B, L, H, d, grid = w.B, w.L, w.H, w.d, w.grid
     scale = 1.0 / math.sqrt(d)
@@ -463,22 +468,26 @@ def run_ours(args, rank, world, local):
         hbm_phases["rope_rotate_kernel"] = {"pass": f"K rotation of {w.name} ({w.L} x {w.H})",
                                             "ms": round(med["rope_ms"], 4), "bytes": c.rope_bytes,
                                             "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4)}
-    if w.kind == "conv3d":
+    if w.kind in CONV_KINDS:
+        down = w.kind == "time_down"
+        x_mib = c.inputs[0].numel() * 2 / 2**20
         config = {"workload": w.name, "kind": w.kind, "B": w.B, "frames": w.T, "height": w.H, "width": w.W,
-                  "c_in": w.c_in, "c_out": w.c_out, "kernel": [3, 3, 3],
-                  "cache": "2 frames of the previous chunk, written for the next one", "flop_per_step": c.flops,
-                  "l2": f"input x {c.inputs[0].numel() * 2 / 2**20:.0f} MiB > L2 126 MB (no flush needed)",
+                  "c_in": w.c_in, "c_out": w.c_out, "kernel": [3, 1, 1] if down else [3, 3, 3],
+                  "cache": f"{1 if down else 2} frame(s) of the previous chunk, written for the next one",
+                  "flop_per_step": c.flops,
+                  "l2": (f"input x {x_mib:.0f} MiB > L2 126 MB (no flush needed)" if x_mib * 2**20 > 126e6 else
+                         f"input x {x_mib:.0f} MiB fits L2 126 MB (not flushed)"),
                   "frac_of_2.25PF_spec": round(value / 2250.0, 4)}
     else:
         config = {"workload": w.name, "kind": w.kind, "B": w.B, "grid": list(w.grid), "tokens": w.L, "heads": w.H,
                   "head_dim": w.d, "flop_per_step": c.flops,
                   "l2": f"inputs {c.in_bytes / 2**30:.2f} GiB > L2 126 MB (no flush needed)",
                   "frac_of_2.25PF_spec": round(value / 2250.0, 4)}
-    if w.kind not in ("cross_fwd", "conv3d"):
+    if w.kind not in ("cross_fwd",) + CONV_KINDS:
         config["theta"] = 10000.0
     config.update(getattr(c, "extra_config", {}))
     line = {
-        "metric": CONV_METRIC if w.kind == "conv3d" else METRIC,
+        "metric": CONV_METRIC if w.kind in CONV_KINDS else METRIC,
         "value": round(value, 2),
         "unit": "TFLOP/s",
         "n_gpus": world,
@@ -489,8 +498,8 @@ def run_ours(args, rank, world, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": getattr(c, "dtype", "bf16"),
-        "data": ("synthetic: bf16 N(0,1) activations and cache, N(0,1)/sqrt(27 C_in) weights (torch generator, "
-                 "seed 1000*(s+1)+rank for input seeds s)" if w.kind == "conv3d" else
+        "data": (f"synthetic: bf16 N(0,1) activations and cache, N(0,1)/sqrt({w.taps()} C_in) weights (torch "
+                 "generator, seed 1000*(s+1)+rank for input seeds s)" if w.kind in CONV_KINDS else
                  "synthetic: bf16 N(0,1) inputs (torch generator, seed 1000*(s+1)+rank for input seeds s)"),
         "config": config,
         "roofline": roofline,
@@ -550,6 +559,9 @@ def extras(wan, torch, dev, peaks, skip=None):
     from long_sequence_attention_02_b300.workloads import CONV_WORKLOADS
 
     w = CONV_WORKLOADS["wan_vae_conv3d_360x640_192"]
+    if w.name != skip:
+        _extra_conv(wan, torch, dev, w, stream, timeit, out, peaks)
+    w = CONV_WORKLOADS["wan_vae_time_down_180x320_192"]
     if w.name != skip:
         _extra_conv(wan, torch, dev, w, stream, timeit, out, peaks)
     return out
@@ -689,6 +701,13 @@ def _extra_conv(wan, torch, dev, w, stream, timeit, out, peaks):
     out[w.name] = {"ms": round(tot, 3), "tflops": round(w.flops() / tot / 1e9, 1),
                    "kernel_tflops": round(w.flops() / ker / 1e9, 1),
                    "kernel_frac_of_bf16_sustained": round(w.flops() / ker / 1e9 / peaks["bf16_tflops_sustained"], 4)}
+    if w.kind == "time_down":
+        # Compulsory bytes of the kernel: x and the cache read once, y written once, the weights.
+        io = (w.B * (w.T + 1) * w.H * w.W * w.c_in + w.B * w.t_out() * w.H * w.W * w.c_out
+              + 3 * w.c_in * w.c_out) * 2
+        out[w.name].update({"kernel_bytes": io, "kernel_gbs": round(io / ker / 1e6, 1),
+                            "kernel_frac_of_hbm": round(io / ker / 1e6 / peaks["hbm_gbs"], 4),
+                            "note": "inputs (89 MB) fit L2; between HBM and tensor bound"})
     del c
 
 
@@ -753,30 +772,37 @@ def _oracle_rows(w, rows_per_head: int, heads: int, seed: int = 0):
 
 def _oracle_conv(w, n_pos: int, seed: int = 0):
     """Time the conv oracle on n_pos output positions, each computed from its
-    3 x 3 x 3 window (drawn from the seeded generator) against all C_out.
-    Returns (positions, seconds, FLOP per position)."""
+    3 x 3 x 3 window (3 x 1 x 1 for the time-downsampling layer: one cached
+    frame and two chunk frames), drawn from the seeded generator, against all
+    C_out. Returns (positions, seconds, FLOP per position)."""
     import numpy as np
 
     from long_sequence_attention_02_b300 import synth
     from oracle import vae
 
-    ci, co = w.c_in, w.c_out
-    wt = synth.bf16_bits_to_f64(synth.normal_bf16(seed, synth.STREAM_V, (co, 3, 3, 3, ci))) / math.sqrt(27 * ci)
+    ci, co, taps = w.c_in, w.c_out, w.taps()
+    shape = (co, 3, ci) if w.kind == "time_down" else (co, 3, 3, 3, ci)
+    wt = synth.bf16_bits_to_f64(synth.normal_bf16(seed, synth.STREAM_V, shape)) / math.sqrt(taps * ci)
     rng = np.random.default_rng(seed)
     t0 = time.perf_counter()
     for i in range(n_pos):
-        off = int(rng.integers(0, 2**40)) * 27 * ci
-        win = synth.bf16_bits_to_f64(synth.normal_bf16(seed, synth.STREAM_Q, (1, 3, 3, 3, ci), offset=off))
-        vae.causal_conv3d_at(win, wt, None, None, [(0, 2, 1, 1)])
+        off = int(rng.integers(0, 2**40)) * taps * ci
+        if w.kind == "time_down":
+            win = synth.bf16_bits_to_f64(synth.normal_bf16(seed, synth.STREAM_Q, (1, 3, 1, 1, ci), offset=off))
+            vae.causal_time_downsample(win[:, 1:], wt, None, win[:, :1])
+        else:
+            win = synth.bf16_bits_to_f64(synth.normal_bf16(seed, synth.STREAM_Q, (1, 3, 3, 3, ci), offset=off))
+            vae.causal_conv3d_at(win, wt, None, None, [(0, 2, 1, 1)])
     dt = time.perf_counter() - t0
-    return n_pos, dt, 2.0 * 27 * ci * co
+    return n_pos, dt, 2.0 * taps * ci * co
 
 
 def cpu_baseline(w, rows_per_head: int):
-    if w.kind == "conv3d":
+    if w.kind in CONV_KINDS:
         n, dt, per = _oracle_conv(w, 2 * rows_per_head)
+        win = "3x1x1" if w.kind == "time_down" else "3x3x3"
         return {"value": round(per * n / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                "sample": f"{n} output positions of {w.name}, each from its 3x3x3 window against all {w.c_out} "
+                "sample": f"{n} output positions of {w.name}, each from its {win} window against all {w.c_out} "
                           f"output channels, fp64 numpy, {dt:.1f} s", "positions_per_s": round(n / dt, 1)}
     n, dt, per_row = _oracle_rows(w, rows_per_head, heads=2)
     what = {"self_fwd": "forward", "self_fwd_fp8": "forward", "cross_fwd": "cross-attention forward",
@@ -841,7 +867,8 @@ def run_reference_conv(args, world):
         "config": {"workload": w.name, "kind": w.kind, "B": w.B, "frames": w.T, "height": w.H, "width": w.W,
                    "c_in": w.c_in, "c_out": w.c_out},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                         "sample": f"{n} output positions per step, each from its 3x3x3 window (fp64 numpy oracle)"},
+                         "sample": f"{n} output positions per step, each from its "
+                                   f"{'3x1x1' if w.kind == 'time_down' else '3x3x3'} window (fp64 numpy oracle)"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

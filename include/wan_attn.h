@@ -303,6 +303,38 @@ int wan_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, f
 int wan_vae_causal_conv3d(const void* x, const void* cache, const void* weight, const float* bias, void* y,
                           void* cache_out, int B, int T, int H, int W, int c_in, int c_out, void* stream);
 
+/*
+ * One time-downsampling layer of the Wan-VAE encoder on one chunk of frames,
+ * with its one-frame feature cache (gojay.top "Wan2.1" reading, Feature
+ * Cache section and Fig. vae_cache (b): a causal temporal convolution of
+ * stride 2 whose cache holds the previous chunk's last input frame, so that
+ * chunks of 1, 4, 4, ... frames give the same outputs as the whole video).
+ * Readings: the kernel is 3 frames x 1 x 1 pixels with no padding; a first
+ * chunk is one frame and passes through unchanged.
+ *
+ *   later chunk (cache given, T even):
+ *     y[b,t,h,w,o] = bias[o] + sum_{kt,c} weight[o,kt,c] * xq[b, 2t+kt, h, w, c],
+ *     t < T/2, xq = cache ++ x in time;
+ *   first chunk (cache NULL): T must be 1 and c_out == c_in; y = x.
+ *
+ *   x         : [B, T, H, W, c_in]  bf16, channels last (device)
+ *   cache     : [B, 1, H, W, c_in]  bf16, the previous chunk's last input
+ *               frame, or NULL for a first chunk
+ *   weight    : [c_out, 3, c_in] bf16 (not read for a first chunk; may be NULL there)
+ *   bias      : [c_out] fp32, or NULL (not read for a first chunk)
+ *   y         : [B, T/2, H, W, c_out] bf16 for a later chunk, [B, 1, H, W, c_in]
+ *               for a first one (output; must not overlap the inputs)
+ *   cache_out : [B, 1, H, W, c_in] bf16, receives x's last frame for the next
+ *               chunk; may be NULL, and may be the same buffer as cache (it is
+ *               written after the convolution has read cache, in stream order)
+ * c_in and c_out must be multiples of 32 (WAN_ERR_UNSUPPORTED otherwise); an
+ * odd T with a cache, or a first chunk of T != 1 or c_out != c_in, is
+ * WAN_ERR_INVALID. bf16 pointers 16-byte aligned, bias 4-byte aligned. B = 0
+ * is a no-op. fp32 accumulation on tensor cores; y is rounded to bf16.
+ */
+int wan_vae_time_downsample(const void* x, const void* cache, const void* weight, const float* bias, void* y,
+                            void* cache_out, int B, int T, int H, int W, int c_in, int c_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -35,7 +35,7 @@ EXPORTED = (
     "wan_attn_workspace_size", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
     "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall", "wan_attn_fwd_noalloc",
     "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual", "wan_attn_fwd_fp8", "wan_vae_causal_conv3d",
-    "wan_profile_set_pass_events",
+    "wan_profile_set_pass_events", "wan_vae_time_downsample",
 )
 WAN_PASS_MAIN = 0
 WAN_PASS_ROPE = 1
@@ -84,6 +84,7 @@ def load_library(path: str = LIB_PATH):
     lib.wan_xattn_fwd_dual.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, i32, vp, vp, i32, wan_grid_t, i32, i32,
                                        f32, vp]
     lib.wan_vae_causal_conv3d.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
+    lib.wan_vae_time_downsample.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     lib.wan_get_device_status.argtypes = [vp]
     lib.wan_debug_inject_stall.argtypes = [i32, i32]
     lib.wan_profile_set_events.argtypes = [vp, vp]
@@ -91,7 +92,7 @@ def load_library(path: str = LIB_PATH):
     for name in ("wan_rope3d_tables", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
                  "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall",
                  "wan_attn_fwd_noalloc", "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual", "wan_attn_fwd_fp8",
-                 "wan_vae_causal_conv3d", "wan_profile_set_pass_events"):
+                 "wan_vae_causal_conv3d", "wan_profile_set_pass_events", "wan_vae_time_downsample"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -186,6 +187,11 @@ def wan_attn_fwd_fp8(q, k, v, o, lse, B, grid, H, head_dim, tables, scale, works
 def wan_vae_causal_conv3d(x, cache, weight, bias, y, cache_out, B, T, H, W, c_in, c_out, stream=None) -> int:
     return load_library().wan_vae_causal_conv3d(_ptr(x), _ptr(cache), _ptr(weight), _ptr(bias), _ptr(y),
                                                  _ptr(cache_out), B, T, H, W, c_in, c_out, _stream(stream))
+
+
+def wan_vae_time_downsample(x, cache, weight, bias, y, cache_out, B, T, H, W, c_in, c_out, stream=None) -> int:
+    return load_library().wan_vae_time_downsample(_ptr(x), _ptr(cache), _ptr(weight), _ptr(bias), _ptr(y),
+                                                   _ptr(cache_out), B, T, H, W, c_in, c_out, _stream(stream))
 
 
 def wan_attn_fwd_ring_step(q, k, v, o, lse, B, grid, H, head_dim, tables, scale, q_start, q_len, kv_start, kv_len,
@@ -326,4 +332,26 @@ def causal_conv3d(x, weight, bias=None, cache=None, stream=None):
     new_cache = torch.empty(B, 2, H, W, c_in, dtype=torch.bfloat16, device=x.device)
     check(wan_vae_causal_conv3d(x, cache, weight, bias, y, new_cache, B, T, H, W, c_in, c_out, stream),
           "wan_vae_causal_conv3d")
+    return y, new_cache
+
+
+def time_downsample(x, weight, bias=None, cache=None, stream=None):
+    """One time-downsampling layer (3 x 1 x 1 taps, stride 2 in time) of the
+    Wan-VAE encoder on one chunk of frames.
+
+    x: bf16 [B, T, H, W, C_in] on the GPU; weight: bf16 [C_out, 3, C_in];
+    bias: fp32 [C_out] or None; cache: bf16 [B, 1, H, W, C_in] from the
+    previous chunk, or None for a first chunk (one frame, passed through).
+    Returns (y [B, T/2, H, W, C_out] (x itself for a first chunk), the cache
+    for the next chunk).
+    """
+    import torch
+
+    B, T, H, W, c_in = x.shape
+    c_out = c_in if cache is None else weight.shape[0]
+    t_out = T if cache is None else T // 2
+    y = torch.empty(B, t_out, H, W, c_out, dtype=torch.bfloat16, device=x.device)
+    new_cache = torch.empty(B, 1, H, W, c_in, dtype=torch.bfloat16, device=x.device)
+    check(wan_vae_time_downsample(x, cache, weight, bias, y, new_cache, B, T, H, W, c_in, c_out, stream),
+          "wan_vae_time_downsample")
     return y, new_cache

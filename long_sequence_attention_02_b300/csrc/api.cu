@@ -438,6 +438,56 @@ int wan_vae_causal_conv3d(const void* x, const void* cache, const void* weight, 
   return WAN_OK;
 }
 
+int wan_vae_time_downsample(const void* x, const void* cache, const void* weight, const float* bias, void* y,
+                            void* cache_out, int B, int T, int H, int W, int c_in, int c_out, void* stream) {
+  if (B < 0 || T <= 0 || H <= 0 || W <= 0 || c_in <= 0 || c_out <= 0 || B > 65535 || T > 65535 || H > 65535 ||
+      W > 65535)
+    return WAN_ERR_INVALID;
+  // A first chunk is one frame and passes through; later chunks are even.
+  if (cache ? T % 2 != 0 : (T != 1 || c_out != c_in)) return WAN_ERR_INVALID;
+  if (c_in % 32 != 0 || c_in > 8192 || c_out > 8192 || wan::conv3d_n_tile(c_out) == 0) return WAN_ERR_UNSUPPORTED;
+  if (B == 0) return WAN_OK;
+  if (!x || !y || (cache && !weight)) return WAN_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(y) || (weight && !aligned16(weight)) || (cache && !aligned16(cache)) ||
+      (cache_out && !aligned16(cache_out)) || (reinterpret_cast<uintptr_t>(bias) & 3u))
+    return WAN_ERR_INVALID;
+  const size_t frame = (size_t)H * W * c_in * 2;  // bytes of one input frame
+  const int t_out = cache ? T / 2 : 1;
+  const size_t x_bytes = (size_t)B * T * frame, c_bytes = (size_t)B * frame;
+  const size_t y_bytes = (size_t)B * t_out * H * W * c_out * 2, w_bytes = (size_t)c_out * 3 * c_in * 2;
+  auto overlap = [](const void* p, size_t n, const void* q, size_t m) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return p && q && a < b + m && b < a + n;
+  };
+  if (overlap(y, y_bytes, x, x_bytes) || (cache && overlap(y, y_bytes, weight, w_bytes)) ||
+      overlap(y, y_bytes, cache, c_bytes) || overlap(cache_out, c_bytes, x, x_bytes) ||
+      overlap(cache_out, c_bytes, y, y_bytes) || (cache_out != cache && overlap(cache_out, c_bytes, cache, c_bytes)))
+    return WAN_ERR_INVALID;
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != WAN_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cache) {
+    rc = wan::launch_causal_conv3d(x, cache, weight, bias, y, B, T, H, W, c_in, c_out, launch_common(*st), s,
+                                   /*time_down=*/true);
+    if (rc != WAN_OK) return rc;
+  } else if (cudaMemcpyAsync(y, x, x_bytes, cudaMemcpyDeviceToDevice, s) != cudaSuccess) {
+    return WAN_ERR_CUDA;
+  }
+  if (cache_out == nullptr) return WAN_OK;
+  // Next chunk's cache: the chunk's last input frame, written after the
+  // convolution has read cache (cache_out may be that buffer).
+  const uint8_t* xb = static_cast<const uint8_t*>(x);
+  uint8_t* ob = static_cast<uint8_t*>(cache_out);
+  if (T == 1)
+    return cudaMemcpyAsync(ob, xb, x_bytes, cudaMemcpyDeviceToDevice, s) == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
+  for (int b = 0; b < B; ++b)
+    if (cudaMemcpyAsync(ob + (size_t)b * frame, xb + ((size_t)b * T + T - 1) * frame, frame,
+                        cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return WAN_ERR_CUDA;
+  return WAN_OK;
+}
+
 int wan_debug_inject_stall(int count, int timeout_ms) {
   if (count < 0 || timeout_ms < 1 || timeout_ms > 10000) return WAN_ERR_INVALID;
   std::lock_guard<std::mutex> lk(g_mu);

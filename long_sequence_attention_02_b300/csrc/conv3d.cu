@@ -28,6 +28,11 @@
 // The CTAs are persistent (one per SM) and keep two accumulators in TMEM,
 // so that one tile's epilogue runs under the next tile's MMAs.
 // Every wait is bounded; on a timeout the device error word is set.
+//
+// The same kernel, instantiated with kTimeDown, runs the encoder's
+// time-downsampling layer (Fig. vae_cache (b)): 3 x 1 x 1 taps, stride 2 in
+// time, a one-frame cache, K = 3 taps x C_in; output frame t of a chunk
+// reads its input frames 2t - 1 (the cache for t = 0), 2t and 2t + 1.
 #include <climits>
 
 #include "common.cuh"
@@ -128,7 +133,11 @@ __device__ __forceinline__ uint64_t conv_desc(uint32_t saddr) {
 // blockIdx.x + gridDim.x, ... The ring of {A, B} stages runs on across
 // tiles, and TMEM holds two accumulators, so the epilogue of one tile
 // overlaps the MMAs of the next.
-template <int kC>
+//
+// kTimeDown selects the time-downsampling layer (Fig. vae_cache (b)): 3 x 1 x
+// 1 taps with stride 2 in time; output frame t reads frames 2t - 1, 2t and
+// 2t + 1 of the chunk, frame -1 being the one cached frame.
+template <int kC, bool kTimeDown>
 __global__ void __launch_bounds__(kConvThreads, 1)
     causal_conv3d_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_cache,
                          const __grid_constant__ CUtensorMap tm_w, const ConvArgs a) {
@@ -148,8 +157,9 @@ __global__ void __launch_bounds__(kConvThreads, 1)
   const int lane = threadIdx.x & 31;
   volatile int* abort = &abort_sh;
   const uint64_t to = a.lc.timeout_ns;
+  constexpr int kTaps = kTimeDown ? 3 : 27;
   const int c_steps = a.c_in / kC;
-  const int k_steps = 27 * c_steps;
+  const int k_steps = kTaps * c_steps;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesC; ++s) {
@@ -192,12 +202,15 @@ __global__ void __launch_bounds__(kConvThreads, 1)
           if (a.lc.stall && g == 2) continue;  // test hook: the second K step never arrives
           const int tap = k / c_steps;
           const int c0 = (k % c_steps) * kC;
-          const int kt = tap / 9, kh = (tap / 3) % 3, kw = tap % 3;
-          const int ti = x.t + kt - 2;  // input frame of this tap, < 0 before the chunk
+          const int kt = kTimeDown ? tap : tap / 9;
+          const int kh = kTimeDown ? 1 : (tap / 3) % 3, kw = kTimeDown ? 1 : tap % 3;
+          // input frame of this tap, < 0 before the chunk (the cache holds its last 2 or 1 frames)
+          const int ti = kTimeDown ? 2 * x.t + kt - 1 : x.t + kt - 2;
+          const int cache_frames = kTimeDown ? 1 : 2;
           uint8_t* sa = smem + slot * kStageC;
           mbar_arrive_expect_tx(&bar_full[slot], tx);
           if (ti < 0 && a.has_cache)
-            tma_load_5d(sa, &tm_cache, &bar_full[slot], c0, x.w0 + kw - 1, x.h0 + kh - 1, ti + 2, x.b);
+            tma_load_5d(sa, &tm_cache, &bar_full[slot], c0, x.w0 + kw - 1, x.h0 + kh - 1, ti + cache_frames, x.b);
           else  // before a first chunk (ti < 0) the box lies outside x and reads zeros
             tma_load_5d(sa, &tm_x, &bar_full[slot], c0, x.w0 + kw - 1, x.h0 + kh - 1, ti, x.b);
           tma_load_3d(sa + kATile, &tm_w, &bar_full[slot], c0, tap, x.n0);
@@ -322,12 +335,12 @@ bool make_tmap_act(CUtensorMap* map, const void* base, int B, int frames, int H,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Weights [C_out, 27, C_in] -> 3D tiled map, box {kc c, 1 tap, n_tile rows}.
-bool make_tmap_wt(CUtensorMap* map, const void* base, int c_in, int c_out, int n_tile, int kc) {
+// Weights [C_out, taps, C_in] -> 3D tiled map, box {kc c, 1 tap, n_tile rows}.
+bool make_tmap_wt(CUtensorMap* map, const void* base, int c_in, int c_out, int taps, int n_tile, int kc) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)c_in, 27, (cuuint64_t)c_out};
-  cuuint64_t strides[2] = {(cuuint64_t)c_in * 2, (cuuint64_t)c_in * 2 * 27};
+  cuuint64_t dims[3] = {(cuuint64_t)c_in, (cuuint64_t)taps, (cuuint64_t)c_out};
+  cuuint64_t strides[2] = {(cuuint64_t)c_in * 2, (cuuint64_t)c_in * 2 * taps};
   cuuint32_t box[3] = {(cuuint32_t)kc, 1, (cuuint32_t)n_tile};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -346,7 +359,7 @@ int conv3d_n_tile(int c_out) {
 }
 
 int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const float* bias, void* y, int B, int T,
-                         int H, int W, int c_in, int c_out, const LaunchCommon& lc, cudaStream_t s) {
+                         int H, int W, int c_in, int c_out, const LaunchCommon& lc, cudaStream_t s, bool time_down) {
   const int n_tile = conv3d_n_tile(c_out);
   if (n_tile == 0 || c_in % 32 != 0) return WAN_ERR_UNSUPPORTED;
   const int kc = c_in % 64 == 0 ? 64 : 32;  // input channels per K step
@@ -354,7 +367,7 @@ int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const
   a.bias = bias;
   a.y = static_cast<__nv_bfloat16*>(y);
   a.B = B;
-  a.T = T;
+  a.T = time_down ? T / 2 : T;  // output frames
   a.H = H;
   a.W = W;
   a.c_in = c_in;
@@ -367,7 +380,7 @@ int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const
   a.lc = lc;
   // Two accumulators of n_tile fp32 columns; TMEM is allocated in powers of two.
   a.tmem_cols = 2 * n_tile <= 128 ? 128u : (2 * n_tile <= 256 ? 256u : 512u);
-  const long long total = (long long)B * T * a.tiles_h * a.tiles_w * a.tiles_n;
+  const long long total = (long long)B * a.T * a.tiles_h * a.tiles_w * a.tiles_n;
   if (total > INT_MAX) return WAN_ERR_INVALID;
   a.n_tiles_total = (int)total;
   int dev = 0, sms = 148;
@@ -377,11 +390,13 @@ int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const
   const int grid = (int)(total < sms ? total : sms);  // persistent: one CTA per SM
 
   CUtensorMap tx, tc, tw;
+  const int cache_frames = time_down ? 1 : 2;
   if (!make_tmap_act(&tx, x, B, T, H, W, c_in, kc) ||
-      !make_tmap_act(&tc, cache ? cache : x, B, cache ? 2 : T, H, W, c_in, kc) ||
-      !make_tmap_wt(&tw, wt, c_in, c_out, n_tile, kc))
+      !make_tmap_act(&tc, cache ? cache : x, B, cache ? cache_frames : T, H, W, c_in, kc) ||
+      !make_tmap_wt(&tw, wt, c_in, c_out, time_down ? 3 : 27, n_tile, kc))
     return WAN_ERR_CUDA;
-  auto kern = kc == 64 ? causal_conv3d_kernel<64> : causal_conv3d_kernel<32>;
+  auto kern = time_down ? (kc == 64 ? causal_conv3d_kernel<64, true> : causal_conv3d_kernel<32, true>)
+                        : (kc == 64 ? causal_conv3d_kernel<64, false> : causal_conv3d_kernel<32, false>);
   const int smem = kc == 64 ? ConvCfg<64>::kSmem : ConvCfg<32>::kSmem;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return WAN_ERR_CUDA;

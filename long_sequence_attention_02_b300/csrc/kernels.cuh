@@ -90,8 +90,11 @@ int launch_attn_bwd(const void* q, const void* k, const void* v, const void* o, 
 
 // Causal 3 x 3 x 3 Conv3d of the Wan-VAE on one chunk (conv3d.cu). cache may
 // be null (zeros before the chunk). c_in % 32 == 0; conv3d_n_tile(c_out) > 0.
+// time_down: the 3 x 1 x 1, time-stride-2 downsampling layer instead (T even,
+// a one-frame cache that must be given; T / 2 output frames).
 int conv3d_n_tile(int c_out);
 int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const float* bias, void* y, int B, int T,
-                         int H, int W, int c_in, int c_out, const LaunchCommon& lc, cudaStream_t s);
+                         int H, int W, int c_in, int c_out, const LaunchCommon& lc, cudaStream_t s,
+                         bool time_down = false);
 
 }  // namespace wan

@@ -81,11 +81,17 @@ class ConvWorkload:
     W: int
     c_in: int
     c_out: int
-    kind: str = "conv3d"
+    kind: str = "conv3d"   # or "time_down": the 3 x 1 x 1, time-stride-2 layer (T input frames)
+
+    def t_out(self) -> int:
+        return self.T // 2 if self.kind == "time_down" else self.T
+
+    def taps(self) -> int:
+        return 3 if self.kind == "time_down" else 27
 
     def flops(self) -> float:
-        """2 FLOP per multiply-add: 2 * outputs * C_out * 27 * C_in."""
-        return 2.0 * self.B * self.T * self.H * self.W * self.c_out * 27 * self.c_in
+        """2 FLOP per multiply-add: 2 * outputs * C_out * taps * C_in."""
+        return 2.0 * self.B * self.t_out() * self.H * self.W * self.c_out * self.taps() * self.c_in
 
 
 CONV_WORKLOADS = {
@@ -95,4 +101,11 @@ CONV_WORKLOADS = {
     "wan_vae_conv3d_360x640_192": ConvWorkload("wan_vae_conv3d_360x640_192", 1, 4, 360, 640, 192, 192),
     # 4 frames of 720 x 1280 (full 720p), 96 -> 96: an outer stage, reduced in 32-channel K steps
     "wan_vae_conv3d_720x1280_96": ConvWorkload("wan_vae_conv3d_720x1280_96", 1, 4, 720, 1280, 96, 96),
+    # The encoder's two time-downsampling layers for a 720p chunk of 4 frames
+    # (the spatial 2x stages halve 720 x 1280 first): 4 -> 2 frames of
+    # 180 x 320 at 192 channels, then 2 -> 1 frame of 90 x 160 at 384.
+    "wan_vae_time_down_180x320_192": ConvWorkload("wan_vae_time_down_180x320_192", 1, 4, 180, 320, 192, 192,
+                                                  kind="time_down"),
+    "wan_vae_time_down_90x160_384": ConvWorkload("wan_vae_time_down_90x160_384", 1, 2, 90, 160, 384, 384,
+                                                 kind="time_down"),
 }

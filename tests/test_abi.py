@@ -225,3 +225,31 @@ def test_conv3d_rejects_bad_arguments(lib):
     assert call(cache_out=X) == wan.WAN_ERR_INVALID          # next cache over the input
     assert call(cache_out=C + 64) == wan.WAN_ERR_INVALID     # partly over the cache it reads
     assert call(B=0, x=None, weight=None, y=None) == wan.WAN_OK
+
+
+def test_time_downsample_rejects_bad_arguments(lib):
+    # x [1, 4, 8, 16, 64], y [1, 2, 8, 16, 128], cache [1, 1, 8, 16, 64], weight [128, 3, 64]
+    frame = 8 * 16 * 64 * 2
+    X, Y, C, Wt = FAKE, FAKE + (1 << 24), FAKE + (2 << 24), FAKE + (3 << 24)
+    ok = dict(x=X, cache=C, weight=Wt, bias=FAKE + (4 << 24), y=Y, cache_out=C, B=1, T=4, H=8, W=16, c_in=64,
+              c_out=128, stream=0)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return wan.wan_vae_time_downsample(**a)
+
+    assert call(x=None) == wan.WAN_ERR_INVALID
+    assert call(weight=None) == wan.WAN_ERR_INVALID          # a later chunk needs its weights
+    assert call(y=None) == wan.WAN_ERR_INVALID
+    assert call(x=X + 8) == wan.WAN_ERR_INVALID
+    assert call(bias=FAKE + 2) == wan.WAN_ERR_INVALID
+    assert call(T=3) == wan.WAN_ERR_INVALID                  # later chunks hold an even number of frames
+    assert call(cache=None, cache_out=None) == wan.WAN_ERR_INVALID         # a first chunk is one frame
+    assert call(cache=None, cache_out=None, T=1) == wan.WAN_ERR_INVALID    # ... and keeps its channels
+    assert call(c_in=80) == wan.WAN_ERR_UNSUPPORTED
+    assert call(c_out=48) == wan.WAN_ERR_UNSUPPORTED
+    assert call(y=X + frame) == wan.WAN_ERR_INVALID          # output overlapping the input
+    assert call(cache_out=X + 3 * frame) == wan.WAN_ERR_INVALID   # next cache over the input
+    assert call(cache_out=C + 64) == wan.WAN_ERR_INVALID     # partly over the cache it reads
+    assert call(B=0, x=None, weight=None, y=None) == wan.WAN_OK

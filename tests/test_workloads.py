@@ -48,8 +48,16 @@ def test_conv_workloads():
     from oracle import vae
 
     for w in workloads.CONV_WORKLOADS.values():
-        assert w.kind == "conv3d" and w.c_in % 32 == 0 and w.c_out % 32 == 0
+        assert w.kind in ("conv3d", "time_down") and w.c_in % 32 == 0 and w.c_out % 32 == 0
         assert w.T <= 4                      # chunks of at most four frames
-        assert w.flops() == vae.conv3d_flops(w.B, w.T, w.H, w.W, w.c_in, w.c_out)
+        if w.kind == "conv3d":
+            assert w.flops() == vae.conv3d_flops(w.B, w.T, w.H, w.W, w.c_in, w.c_out)
+        else:
+            assert w.T % 2 == 0 and w.t_out() == w.T // 2   # later chunks: an even frame count, halved
+            assert w.flops() == vae.time_downsample_flops(w.B, w.T // 2, w.H, w.W, w.c_in, w.c_out)
+    # a 4-frame 720p chunk through both downsampling layers ends as one latent frame
+    d1 = workloads.CONV_WORKLOADS["wan_vae_time_down_180x320_192"]
+    d2 = workloads.CONV_WORKLOADS["wan_vae_time_down_90x160_384"]
+    assert d1.t_out() == d2.T and d2.t_out() == 1 and (d1.H, d1.W) == (2 * d2.H, 2 * d2.W)
     big = workloads.CONV_WORKLOADS["wan_vae_conv3d_360x640_192"]
     assert big.B * big.T * big.H * big.W * big.c_in * 2 > 126 * 2**20   # the timed layer's input exceeds L2
