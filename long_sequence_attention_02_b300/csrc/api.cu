@@ -6,11 +6,23 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "wan_attn.h"
 
 namespace {
+
+// A named NVTX range around a call's launches, so that profilers (nsys, or
+// ncu --nvtx --nvtx-include "wan_attn_fwd/") can attribute and select them.
+// With no tool attached, push and pop return at once.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 using wan::kHeadDim;
 
@@ -172,6 +184,7 @@ size_t wan_rope3d_tables_size(wan_grid_t g, int head_dim) {
 }
 
 int wan_rope3d_tables(wan_grid_t g, int head_dim, double theta, float* tables_dev, void* stream) {
+  const NvtxRange nvtx_range("wan_rope3d_tables");
   long long L = 0;
   if (grid_tokens(g, &L) != WAN_OK) return WAN_ERR_INVALID;
   if (head_dim != kHeadDim) return WAN_ERR_UNSUPPORTED;
@@ -209,6 +222,7 @@ size_t wan_attn_workspace_size(int op, int B, wan_grid_t g, int H, int head_dim)
 int wan_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g, int H,
                  int head_dim, const float* tables, float scale, void* workspace, size_t ws_bytes,
                  void* stream) {
+  const NvtxRange nvtx_range("wan_attn_fwd");
   long long L = 0;
   int rc = grid_tokens(g, &L);
   if (rc == WAN_OK) rc = check_shapes(B, L, H, head_dim);
@@ -225,14 +239,19 @@ int wan_attn_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const wan::RopeTables tab = split_tables(tables, g);
   const wan::LaunchCommon lc = launch_common(*st);
-  wan::record_pass(lc, wan::kPassRope, 0, s);
-  if (wan::launch_rope_rotate_bf16(k, workspace, B, g, H, tab, false, s) != cudaSuccess) return WAN_ERR_CUDA;
-  wan::record_pass(lc, wan::kPassRope, 1, s);
+  {
+    const NvtxRange pass("k_rotate");
+    wan::record_pass(lc, wan::kPassRope, 0, s);
+    if (wan::launch_rope_rotate_bf16(k, workspace, B, g, H, tab, false, s) != cudaSuccess) return WAN_ERR_CUDA;
+    wan::record_pass(lc, wan::kPassRope, 1, s);
+  }
+  const NvtxRange pass("attention");
   return wan::launch_attn_fwd(q, workspace, v, o, lse, B, (int)L, (int)L, H, g, tab, true, nullptr, scale, lc, s);
 }
 
 int wan_xattn_fwd(const void* q, const void* k, const void* v, const int32_t* kv_lens, int Lk, void* o,
                   float* lse, int B, wan_grid_t g, int H, int head_dim, float scale, void* stream) {
+  const NvtxRange nvtx_range("wan_xattn_fwd");
   long long L = 0;
   int rc = grid_tokens(g, &L);
   if (rc == WAN_OK) rc = check_shapes(B, L, H, head_dim);
@@ -253,6 +272,7 @@ int wan_xattn_fwd(const void* q, const void* k, const void* v, const int32_t* kv
 int wan_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
                  void* dq, void* dk, void* dv, int B, wan_grid_t g, int H, int head_dim, const float* tables,
                  float scale, void* workspace, size_t ws_bytes, void* stream) {
+  const NvtxRange nvtx_range("wan_attn_bwd");
   long long L = 0;
   int rc = grid_tokens(g, &L);
   if (rc == WAN_OK) rc = check_shapes(B, L, H, head_dim);
@@ -275,6 +295,7 @@ int wan_attn_bwd(const void* q, const void* k, const void* v, const void* o, con
 int wan_attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g, int H,
                      int head_dim, const float* tables, float scale, void* workspace, size_t ws_bytes,
                      void* stream) {
+  const NvtxRange nvtx_range("wan_attn_fwd_fp8");
   long long L = 0;
   int rc = grid_tokens(g, &L);
   if (rc == WAN_OK) rc = check_shapes(B, L, H, head_dim);
@@ -296,6 +317,7 @@ int wan_attn_fwd_ring_step(const void* q, const void* k, const void* v, void* o,
                            int H, int head_dim, const float* tables, float scale, int q_start, int q_len,
                            int kv_start, int kv_len, int accumulate, void* workspace, size_t ws_bytes,
                            void* stream) {
+  const NvtxRange nvtx_range("wan_attn_fwd_ring_step");
   long long L = 0;
   int rc = grid_tokens(g, &L);
   if (rc == WAN_OK) rc = check_shapes(B, L, H, head_dim);
@@ -315,10 +337,14 @@ int wan_attn_fwd_ring_step(const void* q, const void* k, const void* v, void* o,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const wan::RopeTables tab = split_tables(tables, g);
   const wan::LaunchCommon lc = launch_common(*st);
-  wan::record_pass(lc, wan::kPassRope, 0, s);
-  if (wan::launch_rope_rotate_bf16_rows(k, workspace, B, kv_len, kv_start, g, H, tab, false, s) != cudaSuccess)
-    return WAN_ERR_CUDA;
-  wan::record_pass(lc, wan::kPassRope, 1, s);
+  {
+    const NvtxRange pass("k_rotate");
+    wan::record_pass(lc, wan::kPassRope, 0, s);
+    if (wan::launch_rope_rotate_bf16_rows(k, workspace, B, kv_len, kv_start, g, H, tab, false, s) != cudaSuccess)
+      return WAN_ERR_CUDA;
+    wan::record_pass(lc, wan::kPassRope, 1, s);
+  }
+  const NvtxRange pass("attention");
   return wan::launch_attn_fwd(q, workspace, v, o, lse, B, q_len, kv_len, H, g, tab, true, nullptr, scale, lc, s,
                               q_start, accumulate ? wan::kMergeLse : wan::kMergeNone);
 }
@@ -326,6 +352,7 @@ int wan_attn_fwd_ring_step(const void* q, const void* k, const void* v, void* o,
 int wan_xattn_fwd_dual(const void* q, const void* k_txt, const void* v_txt, const int32_t* lens_txt, int Lk_txt,
                        const void* k_img, const void* v_img, const int32_t* lens_img, int Lk_img, void* o,
                        float* lse, int B, wan_grid_t g, int H, int head_dim, float scale, void* stream) {
+  const NvtxRange nvtx_range("wan_xattn_fwd_dual");
   long long L = 0;
   int rc = grid_tokens(g, &L);
   if (rc == WAN_OK) rc = check_shapes(B, L, H, head_dim);
@@ -373,6 +400,7 @@ int wan_profile_set_events(void* start, void* stop) { return wan_profile_set_pas
 
 int wan_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g,
                          int H, int head_dim, const float* tables, float scale, void* stream) {
+  const NvtxRange nvtx_range("wan_attn_fwd_noalloc");
   long long L = 0;
   int rc = grid_tokens(g, &L);
   if (rc == WAN_OK) rc = check_shapes(B, L, H, head_dim);
@@ -391,6 +419,7 @@ int wan_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* o, f
 
 int wan_vae_causal_conv3d(const void* x, const void* cache, const void* weight, const float* bias, void* y,
                           void* cache_out, int B, int T, int H, int W, int c_in, int c_out, void* stream) {
+  const NvtxRange nvtx_range("wan_vae_causal_conv3d");
   if (B < 0 || T <= 0 || H <= 0 || W <= 0 || c_in <= 0 || c_out <= 0 || B > 65535 || T > 65535 || H > 65535 ||
       W > 65535)
     return WAN_ERR_INVALID;
@@ -440,6 +469,7 @@ int wan_vae_causal_conv3d(const void* x, const void* cache, const void* weight, 
 
 int wan_vae_time_downsample(const void* x, const void* cache, const void* weight, const float* bias, void* y,
                             void* cache_out, int B, int T, int H, int W, int c_in, int c_out, void* stream) {
+  const NvtxRange nvtx_range("wan_vae_time_downsample");
   if (B < 0 || T <= 0 || H <= 0 || W <= 0 || c_in <= 0 || c_out <= 0 || B > 65535 || T > 65535 || H > 65535 ||
       W > 65535)
     return WAN_ERR_INVALID;
