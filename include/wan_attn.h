@@ -53,7 +53,8 @@ enum {
   WAN_ERR_INVALID = 1,     /* null pointer, bad size, misalignment, small workspace */
   WAN_ERR_UNSUPPORTED = 2, /* head_dim != 128, or the device is not sm_103 */
   WAN_ERR_CUDA = 3,        /* a CUDA call or launch failed */
-  WAN_ERR_TIMEOUT = 4      /* a device-side bounded wait expired (reported by wan_get_device_status) */
+  WAN_ERR_TIMEOUT = 4,     /* a device-side bounded wait expired (reported by wan_get_device_status) */
+  WAN_ERR_DEVICE_CHECK = 5 /* a debug build's device-side invariant check failed (likewise) */
 };
 
 enum { WAN_OP_FWD = 0, WAN_OP_BWD = 1, WAN_OP_FWD_FP8 = 2 };
@@ -204,6 +205,26 @@ int wan_xattn_fwd_dual(const void* q, const void* k_txt, const void* v_txt, cons
  * if the synchronisation itself failed.
  */
 int wan_get_device_status(void* stream);
+
+/*
+ * Debug builds. The library built with -DWAN_DEBUG (libwan_attn_debug.so)
+ * checks, inside its kernels, invariants they rely on: 1024-byte aligned
+ * shared-memory bases, the TMEM allocation starting at lane 0 / column 0,
+ * tile coordinates inside the problem, 16-byte aligned TMA inner
+ * coordinates. The first failure is written to the device error word
+ * without a trap; wan_get_device_status then returns WAN_ERR_DEVICE_CHECK
+ * and wan_debug_check_line gives the source line of the failed check.
+ *   wan_debug_build        : 1 for the debug library, 0 for the release one.
+ *   wan_debug_inject_check : test hook; the next `count` kernel launches fail
+ *                            their entry check (and skip no work). Debug
+ *                            builds only: WAN_ERR_UNSUPPORTED otherwise,
+ *                            WAN_ERR_INVALID for count < 0.
+ *   wan_debug_check_line   : the line recorded by the last
+ *                            WAN_ERR_DEVICE_CHECK status (0 if none yet).
+ */
+int wan_debug_build(void);
+int wan_debug_inject_check(int count);
+int wan_debug_check_line(void);
 
 /*
  * Profiling hook: when `start` and `stop` (cudaEvent_t passed as void*) are

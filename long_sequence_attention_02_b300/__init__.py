@@ -17,13 +17,18 @@ import math
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libwan_attn.so")
+RELEASE_LIB_PATH = os.path.join(HERE, "libwan_attn.so")
+DEBUG_LIB_PATH = os.path.join(HERE, "libwan_attn_debug.so")  # built with -DWAN_DEBUG
+# Which build to load: WAN_ATTN_LIB may name another build of the same C ABI
+# (the debug library, for instance); by default the release library.
+LIB_PATH = os.environ.get("WAN_ATTN_LIB") or RELEASE_LIB_PATH
 
 WAN_OK = 0
 WAN_ERR_INVALID = 1
 WAN_ERR_UNSUPPORTED = 2
 WAN_ERR_CUDA = 3
 WAN_ERR_TIMEOUT = 4
+WAN_ERR_DEVICE_CHECK = 5
 WAN_OP_FWD = 0
 WAN_OP_BWD = 1
 WAN_OP_FWD_FP8 = 2
@@ -35,7 +40,8 @@ EXPORTED = (
     "wan_attn_workspace_size", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
     "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall", "wan_attn_fwd_noalloc",
     "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual", "wan_attn_fwd_fp8", "wan_vae_causal_conv3d",
-    "wan_profile_set_pass_events", "wan_vae_time_downsample",
+    "wan_profile_set_pass_events", "wan_vae_time_downsample", "wan_debug_build", "wan_debug_inject_check",
+    "wan_debug_check_line",
 )
 WAN_PASS_MAIN = 0
 WAN_PASS_ROPE = 1
@@ -87,12 +93,16 @@ def load_library(path: str = LIB_PATH):
     lib.wan_vae_time_downsample.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     lib.wan_get_device_status.argtypes = [vp]
     lib.wan_debug_inject_stall.argtypes = [i32, i32]
+    lib.wan_debug_build.argtypes = []
+    lib.wan_debug_inject_check.argtypes = [i32]
+    lib.wan_debug_check_line.argtypes = []
     lib.wan_profile_set_events.argtypes = [vp, vp]
     lib.wan_profile_set_pass_events.argtypes = [i32, vp, vp]
     for name in ("wan_rope3d_tables", "wan_attn_fwd", "wan_xattn_fwd", "wan_attn_bwd",
                  "wan_get_device_status", "wan_profile_set_events", "wan_debug_inject_stall",
                  "wan_attn_fwd_noalloc", "wan_attn_fwd_ring_step", "wan_xattn_fwd_dual", "wan_attn_fwd_fp8",
-                 "wan_vae_causal_conv3d", "wan_profile_set_pass_events", "wan_vae_time_downsample"):
+                 "wan_vae_causal_conv3d", "wan_profile_set_pass_events", "wan_vae_time_downsample",
+                 "wan_debug_build", "wan_debug_inject_check", "wan_debug_check_line"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -233,6 +243,18 @@ def wan_profile_set_pass_events(pass_, start, stop) -> int:
 
 def wan_debug_inject_stall(count: int, timeout_ms: int) -> int:
     return load_library().wan_debug_inject_stall(count, timeout_ms)
+
+
+def wan_debug_build() -> int:
+    return load_library().wan_debug_build()
+
+
+def wan_debug_inject_check(count: int) -> int:
+    return load_library().wan_debug_inject_check(count)
+
+
+def wan_debug_check_line() -> int:
+    return load_library().wan_debug_check_line()
 
 
 def check(status: int, where: str = "") -> None:

@@ -21,6 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 ATTN_SOURCES = ["api.cu", "rope.cu", "rows.cu", "attn_fwd.cu", "attn_fwd_fp8.cu", "attn_bwd.cu", "conv3d.cu"]
 ATTN_HEADERS = ["common.cuh", "kernels.cuh"]
 ATTN_LIB = os.path.join(HERE, "libwan_attn.so")
+# -DWAN_DEBUG: device-side invariant checks write the error word (WAN_ERR_DEVICE_CHECK)
+ATTN_DEBUG_LIB = os.path.join(HERE, "libwan_attn_debug.so")
 SYNTH_LIB = os.path.join(HERE, "libwan_synth.so")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -49,28 +51,33 @@ def build_synth(force: bool = False) -> str:
     return SYNTH_LIB
 
 
-def build_attn(force: bool = False, verbose_ptxas: bool = False, extra=()) -> str:
+def build_attn(force: bool = False, verbose_ptxas: bool = False, extra=(), debug: bool = False) -> str:
     srcs = [os.path.join(CSRC, s) for s in ATTN_SOURCES]
     deps = srcs + [os.path.join(CSRC, h) for h in ATTN_HEADERS] + [os.path.join(INCLUDE, "wan_attn.h")]
-    if not (force or _stale(ATTN_LIB, deps)):
-        return ATTN_LIB
-    tmp = ATTN_LIB + ".tmp"
+    target = ATTN_DEBUG_LIB if debug else ATTN_LIB
+    if debug:
+        extra = (*extra, "-DWAN_DEBUG")
+    if not (force or _stale(target, deps)):
+        return target
+    tmp = target + ".tmp"
     cmd = [_nvcc(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-shared",
            "-Xcompiler", "-fPIC", "-cudart", "static", "--expt-relaxed-constexpr",
            "-I", INCLUDE, "-o", tmp, *srcs, *extra]
     if verbose_ptxas:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.check_call(cmd)
-    os.replace(tmp, ATTN_LIB)
-    return ATTN_LIB
+    os.replace(tmp, target)
+    return target
 
 
 def build_all(force: bool = False) -> None:
     build_synth(force)
     build_attn(force)
+    build_attn(force, debug=True)
 
 
 if __name__ == "__main__":
     build_all(force="--force" in sys.argv)
     print(ATTN_LIB)
+    print(ATTN_DEBUG_LIB)
     print(SYNTH_LIB)

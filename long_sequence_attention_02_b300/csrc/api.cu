@@ -42,6 +42,8 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 int g_stall_launches = 0;
+int g_check_launches = 0;     // wan_debug_inject_check
+int g_last_check_line = 0;    // source line of the last debug check reported
 uint64_t g_stall_timeout_ns = 0;
 cudaEvent_t g_prof[wan::kNumPasses][2] = {};  // profiling hook, one-shot (guarded by g_mu)
 
@@ -115,12 +117,17 @@ wan::LaunchCommon launch_common(const DeviceState& st) {
   lc.err = st.err;
   lc.timeout_ns = kDefaultTimeoutNs;
   lc.stall = 0;
+  lc.force_check = 0;
   std::lock_guard<std::mutex> lk(g_mu);
   for (int p = 0; p < wan::kNumPasses; ++p)
     for (int i = 0; i < 2; ++i) {
       lc.ev[p][i] = g_prof[p][i];
       g_prof[p][i] = nullptr;
     }
+  if (g_check_launches > 0) {
+    --g_check_launches;
+    lc.force_check = 1;
+  }
   if (g_stall_launches > 0) {
     --g_stall_launches;
     lc.stall = 1;
@@ -170,6 +177,7 @@ const char* wan_status_str(int status) {
     case WAN_ERR_UNSUPPORTED: return "WAN_ERR_UNSUPPORTED: head_dim or device not supported";
     case WAN_ERR_CUDA: return "WAN_ERR_CUDA: CUDA call or launch failed";
     case WAN_ERR_TIMEOUT: return "WAN_ERR_TIMEOUT: device-side wait expired";
+    case WAN_ERR_DEVICE_CHECK: return "WAN_ERR_DEVICE_CHECK: a debug build's device-side check failed";
     default: return "unknown wan status";
   }
 }
@@ -385,6 +393,11 @@ int wan_get_device_status(void* stream) {
   if (cudaMemcpy(&v, st->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return WAN_ERR_CUDA;
   if (v != 0 && cudaMemcpy(st->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
     return WAN_ERR_CUDA;
+  if ((v & 0xFF) == wan::kDevCheck) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_last_check_line = v >> 8;
+    return WAN_ERR_DEVICE_CHECK;
+  }
   return v == 0 ? WAN_OK : v;
 }
 
@@ -516,6 +529,27 @@ int wan_vae_time_downsample(const void* x, const void* cache, const void* weight
                         cudaMemcpyDeviceToDevice, s) != cudaSuccess)
       return WAN_ERR_CUDA;
   return WAN_OK;
+}
+
+int wan_debug_build(void) {
+#ifdef WAN_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int wan_debug_inject_check(int count) {
+  if (count < 0) return WAN_ERR_INVALID;
+  if (!wan_debug_build()) return WAN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_check_launches = count;
+  return WAN_OK;
+}
+
+int wan_debug_check_line(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_last_check_line;
 }
 
 int wan_debug_inject_stall(int count, int timeout_ms) {

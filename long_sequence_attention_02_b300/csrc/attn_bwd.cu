@@ -181,6 +181,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base_sh;
+  // Debug builds: the 512 TMEM columns start at lane 0 / column 0.
+  if (threadIdx.x == 0) {
+    WAN_DCHECK(!a.lc.force_check, a.lc.err);
+    WAN_DCHECK(tmem == 0u, a.lc.err);
+    WAN_DCHECK(kv0 < a.L && q_start >= 0 && q_start < nq, a.lc.err);
+  }
   const uint32_t tDV = tmem, tDK = tmem + 128, tS = tmem + 256, tDP = tmem + 384;
 
   const size_t bh = static_cast<size_t>(b) * a.H + h;
@@ -311,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < nq; ++i) {
         const int s = i & 1, use = i >> 1;
         const int qt = i + q_start < nq ? i + q_start : i + q_start - nq;
+        WAN_DCHECK(qt >= 0 && qt < nq, a.lc.err);
         uint8_t* st = smem + kOffStage + s * kStageBytes;
         if (!mbar_wait(&bars[kBarStaged0 + s], use & 1, abort, to)) {
           raise_abort(abort, a.lc.err);

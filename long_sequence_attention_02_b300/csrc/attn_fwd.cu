@@ -182,6 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // depend on the order), so that the CTAs of one head in flight read
     // different K/V tiles.
     x.kv_start = x.n_tiles > 0 ? static_cast<int>((static_cast<long long>(qp) * x.n_tiles) / a.n_qpairs) : 0;
+    WAN_DCHECK(x.b < a.B && x.h < a.H && x.q0 < a.Lq && x.n_tiles * kBlockN < a.Lk + kBlockN &&
+                   (x.n_tiles == 0 || x.kv_start < x.n_tiles),
+               a.lc.err);
     return x;
   };
 
@@ -214,6 +217,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  // Debug builds: the 512 TMEM columns start at lane 0 / column 0, and the
+  // swizzled tiles need a 1024-byte aligned shared-memory base.
+  if (threadIdx.x == 0) {
+    WAN_DCHECK(!a.lc.force_check, a.lc.err);
+    WAN_DCHECK(tmem == 0u, a.lc.err);
+    WAN_DCHECK((smem_u32(smem) & 1023u) == 0u, a.lc.err);
+  }
 
   if (warp >= 8) {
    regs_shrink<kControlRegs>();

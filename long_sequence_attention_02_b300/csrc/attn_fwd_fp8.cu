@@ -248,6 +248,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
     x.b = bh / a.H;
     x.q0 = qp * (kTile * kQTiles);
     x.kv_start = static_cast<int>((static_cast<long long>(qp) * n_tiles) / a.n_qpairs);
+    WAN_DCHECK(x.b < a.B && x.h < a.H && x.q0 < a.L && x.kv_start < n_tiles, a.lc.err);
     return x;
   };
 
@@ -275,6 +276,13 @@ __global__ void __launch_bounds__(kThreads8, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  // Debug builds: the 512 TMEM columns start at lane 0 / column 0, and the
+  // swizzled tiles need a 1024-byte aligned shared-memory base.
+  if (threadIdx.x == 0) {
+    WAN_DCHECK(!a.lc.force_check, a.lc.err);
+    WAN_DCHECK(tmem == 0u, a.lc.err);
+    WAN_DCHECK((smem_u32(smem) & 1023u) == 0u, a.lc.err);
+  }
 
   if (warp >= 8) {
    regs_shrink<kControlRegs8>();

@@ -20,7 +20,24 @@ namespace wan {
 enum DeviceError : int {
   kDevOk = 0,
   kDevTimeout = 4,  // a bounded wait expired (matches WAN_ERR_TIMEOUT)
+  kDevCheck = 5,    // a debug build's invariant check failed (matches WAN_ERR_DEVICE_CHECK)
 };
+
+// Debug builds (-DWAN_DEBUG) check, on the device, invariants the kernels
+// rely on (shared-memory and TMEM bases, tile coordinates, TMA alignment).
+// The first failure is written to the error word as kDevCheck | line << 8,
+// without a trap, so the context stays usable and the host reads it with
+// wan_get_device_status. Release builds compile the checks out.
+#ifdef WAN_DEBUG
+#define WAN_DCHECK(cond, err)                                                               \
+  do {                                                                                      \
+    if (!(cond)) atomicCAS((err), 0, static_cast<int>(::wan::kDevCheck) | (__LINE__ << 8)); \
+  } while (0)
+#else
+#define WAN_DCHECK(cond, err) \
+  do {                        \
+  } while (0)
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

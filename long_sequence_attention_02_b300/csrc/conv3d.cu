@@ -182,6 +182,13 @@ __global__ void __launch_bounds__(kConvThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  // Debug builds: the accumulators start at TMEM lane 0 / column 0, and the
+  // swizzled stages need a 1024-byte aligned shared-memory base.
+  if (threadIdx.x == 0) {
+    WAN_DCHECK(!a.lc.force_check, a.lc.err);
+    WAN_DCHECK(tmem == 0u, a.lc.err);
+    WAN_DCHECK((smem_u32(smem) & 1023u) == 0u, a.lc.err);
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -207,6 +214,11 @@ __global__ void __launch_bounds__(kConvThreads, 1)
           // input frame of this tap, < 0 before the chunk (the cache holds its last 2 or 1 frames)
           const int ti = kTimeDown ? 2 * x.t + kt - 1 : x.t + kt - 2;
           const int cache_frames = kTimeDown ? 1 : 2;
+          // Debug builds: the tile lies in the output, and the TMA inner
+          // coordinate (channels) starts on a 16-byte boundary.
+          WAN_DCHECK(x.b < a.B && x.t < a.T && x.h0 < a.H && x.w0 < a.W && x.n0 + a.n_tile <= a.c_out &&
+                         ((c0 * 2) & 15) == 0 && ti >= -cache_frames,
+                     a.lc.err);
           uint8_t* sa = smem + slot * kStageC;
           mbar_arrive_expect_tx(&bar_full[slot], tx);
           if (ti < 0 && a.has_cache)

@@ -34,6 +34,7 @@ struct LaunchCommon {
   int* err;             // device error word
   uint64_t timeout_ns;  // bound of every device-side wait
   int stall;            // test hook: producer withholds one tile
+  int force_check;      // test hook (debug builds): the kernel's entry check fails
   cudaEvent_t ev[kNumPasses][2];  // profiling hook: {start, stop} around each pass (may be null)
 };
 

@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     assert wan.status_str(0) == "WAN_OK"
-    for code in (1, 2, 3, 4):
+    for code in (1, 2, 3, 4, 5):
         assert wan.status_str(code).startswith("WAN_ERR")
     assert wan.wan_version() >= 100
 
@@ -253,3 +253,23 @@ def test_time_downsample_rejects_bad_arguments(lib):
     assert call(cache_out=X + 3 * frame) == wan.WAN_ERR_INVALID   # next cache over the input
     assert call(cache_out=C + 64) == wan.WAN_ERR_INVALID     # partly over the cache it reads
     assert call(B=0, x=None, weight=None, y=None) == wan.WAN_OK
+
+
+def test_debug_build_exports_every_declared_symbol_and_says_so(lib):
+    """The -DWAN_DEBUG library is the same C ABI; only it accepts the forced
+    device-check hook (host-side calls only, no GPU needed)."""
+    import ctypes
+
+    from long_sequence_attention_02_b300 import build
+
+    dbg = ctypes.CDLL(build.build_attn(debug=True))
+    for name in declared_functions():
+        assert hasattr(dbg, name), name
+    assert dbg.wan_debug_build() == 1
+    assert lib.wan_debug_build() == 0
+    assert lib.wan_debug_inject_check(1) == wan.WAN_ERR_UNSUPPORTED     # release: no checks to force
+    assert dbg.wan_debug_inject_check(-1) == wan.WAN_ERR_INVALID
+    assert dbg.wan_debug_inject_check(0) == wan.WAN_OK
+    assert dbg.wan_debug_check_line() == 0
+    dbg.wan_status_str.restype = ctypes.c_char_p
+    assert dbg.wan_status_str(wan.WAN_ERR_DEVICE_CHECK).decode().startswith("WAN_ERR_DEVICE_CHECK")
