@@ -400,30 +400,63 @@ def run_ours(args, rank, world, local):
     value = aggregate(c.flops, world, ms_max / 1e3) / 1e12
 
     # ----- end to end through the C ABI with host buffers
+    # Every step uploads its inputs from pinned host memory, runs, and reads its
+    # results back. Two device buffer sets let step i+1's upload and step i-1's
+    # download (copy streams) overlap step i's compute, as a serving loop would;
+    # each step's own copies stay inside the timed region, which runs from
+    # before the first upload to the end of the last download.
+    sets = [c, make_case(wan, torch, dev, w, rank, peaks, med["seed"])]
     hin = [t.cpu().pin_memory() for t in c.inputs]
-    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in c.outputs]
+    hout = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in c.outputs] for _ in sets]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def e2e_step():
-        for dst, src in zip(c.inputs, hin):
-            dst.copy_(src, non_blocking=True)
-        c.step()
-        for dst, src in zip(hout, c.outputs):
-            dst.copy_(src, non_blocking=True)
+    def e2e_run(n_steps, start_event=None):
+        comp_done, out_done = [None, None], [None, None]
+        for i in range(n_steps):
+            j = i & 1
+            cs = sets[j]
+            with torch.cuda.stream(s_in):
+                if start_event is not None:
+                    s_in.wait_event(start_event)
+                if comp_done[j] is not None:  # the set's inputs are free once its last compute ended
+                    s_in.wait_event(comp_done[j])
+                for dst, src in zip(cs.inputs, hin):
+                    dst.copy_(src, non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+            stream.wait_event(ev_in)
+            if out_done[j] is not None:  # its outputs are free once read back
+                stream.wait_event(out_done[j])
+            cs.step()
+            comp_done[j] = torch.cuda.Event()
+            comp_done[j].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[j])
+                for dst, src in zip(hout[j], cs.outputs):
+                    dst.copy_(src, non_blocking=True)
+                out_done[j] = torch.cuda.Event()
+                out_done[j].record(s_out)
+        for e in out_done:
+            if e is not None:
+                stream.wait_event(e)
 
-    e2e_steps = max(1, min(args.steps, 5))
-    e2e_step()
+    e2e_steps = max(2, min(args.steps, 10))
+    e2e_run(2)
     torch.cuda.synchronize()
     barrier(world)
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    e2e_run(e2e_steps, a0)
     a1.record(stream)
     torch.cuda.synchronize()
+    wan.check(wan.wan_get_device_status())
     e2e_ms = max_over_ranks(a0.elapsed_time(a1) / e2e_steps, world)
     e2e = {"value": round(aggregate(c.flops, world, e2e_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
-           "h2d_bytes_per_step": c.in_bytes, "d2h_bytes_per_step": c.out_bytes, "ms_per_step": round(e2e_ms, 3)}
-    del hin, hout
+           "h2d_bytes_per_step": c.in_bytes, "d2h_bytes_per_step": c.out_bytes, "ms_per_step": round(e2e_ms, 3),
+           "steps": e2e_steps,
+           "pipelining": "two device buffer sets; uploads and downloads on two copy streams overlap the "
+                         "neighbouring steps' compute"}
+    del hin, hout, sets
 
     also = {}
     if not args.no_extras and rank == 0:
