@@ -209,7 +209,8 @@ def make_conv_case(wan, torch, dev, w, rank, seed=0):
 
     c.inputs, c.outputs = [x, cache, wt, bias], [y, cache_out]
     c.flops = c.kernel_flops = w.flops()
-    c.kernel, c.launches, c.hbm_bytes, c.bound = "causal_conv3d_kernel", 1, None, "tensor"
+    c.kernel = "causal_conv3d_kernel<time_down>" if down else "causal_conv3d_kernel"
+    c.launches, c.hbm_bytes, c.bound = 1, None, "tensor"
 
     def step(prof=None, rope_prof=None):
         if prof is not None:
@@ -754,6 +755,7 @@ KERNEL_SOURCES = {
     "attn_bwd_kernel": ("attn_bwd.cu", "common.cuh"),
     "attn_fwd_fp8_kernel": ("attn_fwd_fp8.cu", "common.cuh"),
     "causal_conv3d_kernel": ("conv3d.cu", "common.cuh"),
+    "causal_conv3d_kernel<time_down>": ("conv3d.cu", "common.cuh"),
 }
 
 
