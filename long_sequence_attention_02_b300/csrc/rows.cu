@@ -19,11 +19,16 @@ namespace {
 // the sums in shared memory; then D and LSE * log2 e go out along the token
 // axis, so that the [B*H][Lpad] rows are read and written 128 bytes at a
 // time rather than one float per row.
+//
+// The pass is short on instructions per byte: with all heads in one pass
+// (H <= kRowsMaxH, every Wan shape) chunk q of the tile is simply chunk q of
+// the tile's contiguous bytes and row q / 16 of its sums, so the loop does
+// no division.
 constexpr int kRowsTok = 32;
 constexpr int kRowsMaxH = 64;  // heads per block tile held in shared memory (larger H: several passes)
 __global__ void __launch_bounds__(256) bwd_rows_kernel(const uint4* o, const uint4* dout, const float* lse,
                                                        float* lse2, float* drow, int B, int L, int Lpad, int H) {
-  __shared__ float dsum[kRowsTok][kRowsMaxH + 1];
+  __shared__ float dsum[kRowsTok * kRowsMaxH];  // [token][head of this pass]
   constexpr int kUnroll = 4;
   const int tiles_l = (L + kRowsTok - 1) / kRowsTok;
   const int c = threadIdx.x & 15;
@@ -35,6 +40,8 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(const uint4* o, const uin
     const int n_tok = L - l0 < kRowsTok ? L - l0 : kRowsTok;
     for (int h0 = 0; h0 < H; h0 += kRowsMaxH) {
       const int nh = H - h0 < kRowsMaxH ? H - h0 : kRowsMaxH;
+      const bool whole = nh == H;  // the tile's rows are contiguous: row r of the pass is row r of the tile
+      const size_t base = (static_cast<size_t>(b) * L + l0) * H * 16;
       const int n = n_tok * nh * 16;  // chunks of this pass
       for (int q0 = threadIdx.x; q0 < n; q0 += kUnroll * 256) {
         uint4 xo[kUnroll], yo[kUnroll];
@@ -43,7 +50,8 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(const uint4* o, const uin
           const int q = q0 + u * 256;
           if (q < n) {
             const int rh = q >> 4;  // (token, head) of this pass
-            const size_t i = ((static_cast<size_t>(b) * L + l0 + rh / nh) * H + h0 + rh % nh) * 16 + c;
+            const size_t i = whole ? base + q
+                                   : ((static_cast<size_t>(b) * L + l0 + rh / nh) * H + h0 + rh % nh) * 16 + c;
             xo[u] = o[i];
             yo[u] = dout[i];
           }
@@ -61,10 +69,7 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(const uint4* o, const uin
           }
 #pragma unroll
           for (int m = 8; m >= 1; m >>= 1) acc += __shfl_xor_sync(group, acc, m, 16);
-          if (c == 0) {
-            const int rh = q >> 4;
-            dsum[rh / nh][rh % nh] = acc;
-          }
+          if (c == 0) dsum[q >> 4] = acc;
         }
       }
       __syncthreads();
@@ -72,7 +77,7 @@ __global__ void __launch_bounds__(256) bwd_rows_kernel(const uint4* o, const uin
         const int hh = e / kRowsTok, t = e % kRowsTok;
         if (t < n_tok) {
           const size_t bh = static_cast<size_t>(b) * H + h0 + hh;
-          drow[bh * Lpad + l0 + t] = dsum[t][hh];
+          drow[bh * Lpad + l0 + t] = dsum[t * nh + hh];
           lse2[bh * Lpad + l0 + t] = lse[bh * L + l0 + t] * 1.4426950408889634f;
         }
       }

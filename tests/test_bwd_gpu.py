@@ -39,6 +39,7 @@ SMALL = [
     (2, (4, 8, 8), 1),     # 256: two full tiles, B = 2
     (1, (8, 16, 16), 2),   # 2048: many tiles both ways
     (2, (5, 13, 17), 1),   # 1105: ragged, odd extents
+    (1, (2, 4, 5), 72),    # 40 tokens, 72 heads: the row pass takes its heads in two passes (64 + 8)
 ]
 
 
