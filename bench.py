@@ -6,8 +6,11 @@ A step is one wan_attn_fwd call (K RoPE pre-pass + attention kernel) on
 inputs already resident in HBM; the RoPE tables are a per-grid constant built
 once before timing. value = 4*B*H*L^2*d / step time (TFLOP/s).
 
-Also reported (same run): the 480p 1.3B self-attention forward, the
-cross-attention forward and the 64^3 training step (forward + backward).
+Also reported (same run, under "also"): the tiny forward's latency, the
+480p 1.3B self-attention forward, the cross-attention forward, the 64^3
+training step (forward + backward), the VAE Conv3d and time-downsampling
+layers, the FP8 forward, the decoupled text + image cross-attention and the
+720p forward as two Ring steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -598,7 +601,96 @@ def extras(wan, torch, dev, peaks, skip=None):
     w = CONV_WORKLOADS["wan_vae_time_down_180x320_192"]
     if w.name != skip:
         _extra_conv(wan, torch, dev, w, stream, timeit, out, peaks)
+    w = WORKLOADS["wan14b_720p_self_fwd_fp8"]
+    if w.name != skip:
+        _extra_fp8(wan, torch, dev, w, stream, timeit, out, peaks)
+    _extra_dual(wan, torch, dev, WORKLOADS["wan14b_720p_cross_fwd"], stream, timeit, out, peaks)
+    _extra_ring(wan, torch, dev, WORKLOADS["wan14b_720p_self_fwd"], stream, timeit, out, peaks)
     return out
+
+
+def _extra_fp8(wan, torch, dev, w, stream, timeit, out, peaks):
+    """FP8 forward of the 75,600-token, 40-head problem: the whole call (amax,
+    quantisation, attention) and its attention kernel."""
+    B, L, H, d = w.B, w.L, w.H, w.d
+    q = torch.randn(B, L, H, d, device=dev).bfloat16()
+    k, v = torch.randn_like(q), torch.randn_like(q)
+    o, lse = torch.empty_like(q), torch.empty(B, H, L, device=dev)
+    tab = wan.rope_tables(w.grid, device=dev)
+    wsb = wan.wan_attn_workspace_size(wan.WAN_OP_FWD_FP8, B, w.grid, H, d)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+
+    def f(p):
+        if p is not None:
+            wan.wan_profile_set_events(*p)
+        wan.check(wan.wan_attn_fwd_fp8(q, k, v, o, lse, B, w.grid, H, d, tab, 1 / math.sqrt(d), ws, wsb, stream))
+
+    tot, ker = timeit(f, iters=3, prof=True)
+    fl = 4.0 * B * H * L * L * d
+    out[w.name] = {"ms": round(tot, 3), "tflops": round(fl / tot / 1e9, 1), "kernel_tflops": round(fl / ker / 1e9, 1),
+                   "kernel_frac_of_fp8_peak": round(fl / ker / 1e9 / (2 * peaks["bf16_tflops"]), 4),
+                   "peak": "fp8 = 2 x the measured bf16 burst (nominal 4.5 / 2.25 PF)"}
+    del q, k, v, o, lse, ws
+
+
+def _extra_dual(wan, torch, dev, w, stream, timeit, out, peaks):
+    """Decoupled text + image cross-attention of image-to-video models on the
+    720p cross-attention shape: 512 text keys (seeded lengths) and 257 image
+    keys (a CLIP ViT-H/14 embedding of 16 x 16 patches + 1; the pages give no
+    count). Two launches; the second adds its result to the first's O."""
+    from long_sequence_attention_02_b300 import synth
+
+    B, Lq, H, d, Lk = w.B, w.L, w.H, w.d, w.Lk
+    Li = 257
+    q = torch.randn(B, Lq, H, d, device=dev).bfloat16()
+    kt, vt = torch.randn(B, Lk, H, d, device=dev).bfloat16(), torch.randn(B, Lk, H, d, device=dev).bfloat16()
+    ki, vi = torch.randn(B, Li, H, d, device=dev).bfloat16(), torch.randn(B, Li, H, d, device=dev).bfloat16()
+    lens_np = synth.kv_lens(0, B)
+    lens = torch.from_numpy(lens_np).to(dev)
+    o, lse = torch.empty_like(q), torch.empty(B, H, Lq, device=dev)
+
+    def f(p):
+        wan.check(wan.wan_xattn_fwd_dual(q, kt, vt, lens, Lk, ki, vi, None, Li, o, lse, B, w.grid, H, d,
+                                          1 / math.sqrt(d), stream))
+
+    tot, _ = timeit(f, iters=10)
+    qb = q.numel() * 2
+    moved = 5 * qb + lse.numel() * 4 + 2 * (kt.numel() + ki.numel()) * 2  # Q twice, O written twice, read once
+    floor = 2 * qb + lse.numel() * 4 + 2 * (kt.numel() + ki.numel()) * 2  # Q read and O written once
+    out["wan14b_720p_xattn_dual_txt512_img257"] = {
+        "ms": round(tot, 3), "tflops_nominal": round(4.0 * B * H * Lq * (Lk + Li) * d / tot / 1e9, 1),
+        "kv_lens_txt": lens_np.tolist(), "image_keys": Li, "bytes_moved": moved,
+        "gbs": round(moved / tot / 1e6, 1), "hbm_frac": round(moved / tot / 1e6 / peaks["hbm_gbs"], 3),
+        "single_pass_floor_ms": round(floor / peaks["hbm_gbs"] / 1e6, 3)}
+    del q, kt, vt, ki, vi, o, lse
+
+
+def _extra_ring(wan, torch, dev, w, stream, timeit, out, peaks):
+    """The 75,600-token, 40-head forward as two Ring steps over the K/V halves
+    (the second merges into the first's O and LSE by log-sum-exp), against the
+    one-call forward's FLOP."""
+    B, L, H, d = w.B, w.L, w.H, w.d
+    q = torch.randn(B, L, H, d, device=dev).bfloat16()
+    k, v = torch.randn_like(q), torch.randn_like(q)
+    o, lse = torch.empty_like(q), torch.empty(B, H, L, device=dev)
+    tab = wan.rope_tables(w.grid, device=dev)
+    wsb = wan.wan_attn_workspace_size(wan.WAN_OP_FWD, B, w.grid, H, d)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    half = L // 2
+    chunks = [(0, half), (half, L - half)]
+    kc = [k[:, a:a + n].contiguous() for a, n in chunks]
+    vc = [v[:, a:a + n].contiguous() for a, n in chunks]
+
+    def f(p):
+        for i, (a, n) in enumerate(chunks):
+            wan.check(wan.wan_attn_fwd_ring_step(q, kc[i], vc[i], o, lse, B, w.grid, H, d, tab, 1 / math.sqrt(d), 0,
+                                                 L, a, n, 1 if i else 0, ws, wsb, stream))
+
+    tot, _ = timeit(f, iters=3)
+    fl = 4.0 * B * H * L * L * d
+    out["wan14b_720p_self_fwd_ring2"] = {"ms": round(tot, 3), "tflops": round(fl / tot / 1e9, 1),
+                                         "steps": 2, "kv_chunk_tokens": half}
+    del q, k, v, o, lse, ws, kc, vc
 
 
 def _extra_tiny(wan, torch, dev, w, stream, out, iters=200):
