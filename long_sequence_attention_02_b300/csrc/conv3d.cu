@@ -24,7 +24,8 @@
 // tcgen05.mma of kind::f16 (K = 16 each) accumulate into TMEM.
 //
 // Warps: 0 TMA producer, 1 MMA issuer and TMEM owner, 2-5 epilogue
-// (TMEM -> + bias -> bf16 -> global, positions inside the picture only).
+// (TMEM -> + bias -> bf16 -> shared memory -> TMA stores of 32 channels,
+// which write only the positions inside the picture).
 // The CTAs are persistent (one per SM) and keep two accumulators in TMEM,
 // so that one tile's epilogue runs under the next tile's MMAs.
 // Every wait is bounded; on a timeout the device error word is set.
@@ -47,6 +48,24 @@ constexpr int kPatchW = 16;                   // 128 output positions per tile
 constexpr int kConvThreads = 192;
 constexpr int kRingBytes = 192 * 1024;        // the {A, B} stage ring
 
+// The epilogue stages 32 output channels of a tile (128 positions x 64 bytes,
+// 64-byte swizzle) for one TMA store; two such buffers alternate.
+constexpr int kOutStage = 128 * 64;
+
+// Byte offset of 16-byte chunk `chunk` (0..3) of row `row` in a 64-byte-row
+// tile in the SWIZZLE_64B layout: chunk bits 4-5 of the address XOR bits 7-8.
+__device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t chunk) {
+  return row * 64u + ((chunk ^ ((row >> 1) & 3u)) << 4);
+}
+
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, const void* src, int c0, int c1, int c2, int c3,
+                                             int c4) {
+  asm volatile("cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4, %5}], [%6];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(src))
+               : "memory");
+}
+
 // One K step covers kC input channels of one tap: 64 (rows of 128 bytes,
 // 128-byte swizzle) when C_in is a multiple of 64, else 32 (rows of 64 bytes,
 // 64-byte swizzle) for layers such as the VAE's 96-channel ones.
@@ -57,7 +76,7 @@ struct ConvCfg {
   static constexpr int kBTileMax = 256 * kRow;         // up to 256 output channels
   static constexpr int kStage = kATile + kBTileMax;    // 48 KB / 24 KB
   static constexpr int kStages = kRingBytes / kStage;  // 4 / 8
-  static constexpr int kSmem = kStages * kStage + 1024;
+  static constexpr int kSmem = kStages * kStage + 2 * kOutStage + 1024;
   static constexpr uint32_t kSwizzle = kC == 64 ? 2u : 4u;  // descriptor layout: SWIZZLE_128B / SWIZZLE_64B
 };
 
@@ -140,7 +159,8 @@ __device__ __forceinline__ uint64_t conv_desc(uint32_t saddr) {
 template <int kC, bool kTimeDown>
 __global__ void __launch_bounds__(kConvThreads, 1)
     causal_conv3d_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_cache,
-                         const __grid_constant__ CUtensorMap tm_w, const ConvArgs a) {
+                         const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_y,
+                         const ConvArgs a) {
   using Cfg = ConvCfg<kC>;
   constexpr int kStagesC = Cfg::kStages;
   constexpr int kATile = Cfg::kATile;
@@ -152,6 +172,7 @@ __global__ void __launch_bounds__(kConvThreads, 1)
   __shared__ __align__(8) uint64_t bar_acc_full[2], bar_acc_empty[2], bar_drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
+  __shared__ int epi_ok[4];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -278,23 +299,31 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     mbar_wait(&bar_drain, 0, nullptr, to);
   } else {
     // ------------------------------------------------------------ epilogue
+    // Per 32 output channels of a tile: TMEM -> + bias -> bf16 -> a swizzled
+    // staging buffer -> one TMA store, which also leaves out the positions
+    // outside the picture. The bias arrives as one coalesced load per warp
+    // (lane l holds channel l) and is spread with shuffles. The four warps
+    // decide together whether to stop (flags written before a named barrier,
+    // read after it), so none is left at a barrier.
     const int q = warp & 3;  // TMEM lanes 32q .. 32q+31
     const int r = q * 32 + lane;
-    int i = 0;
+    const bool leader = warp == 2 && lane == 0;  // issues the stores
+    uint8_t* stage0 = smem + kStagesC * kStageC;
+    int i = 0, nchunk = 0;
     for (int idx = blockIdx.x; idx < a.n_tiles_total; idx += gridDim.x, ++i) {
       const int ab = i & 1;
       const bool done = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full[ab], (i >> 1) & 1, abort, to));
-      if (!done || *abort) {
+      if (lane == 0) epi_ok[warp - 2] = done && !*abort ? 1 : 0;
+      named_bar_sync(1, 128);
+      const bool all_done = epi_ok[0] & epi_ok[1] & epi_ok[2] & epi_ok[3];
+      if (!all_done) {
         if (!done && lane == 0) conv_abort(abort, a.lc.err);
         break;
       }
       tc_fence_after();
       const ConvTile x = conv_tile(idx, a);
-      const int h = x.h0 + r / kPatchW, w = x.w0 + r % kPatchW;
-      const bool inside = h < a.H && w < a.W;
-      __nv_bfloat16* dst = a.y + ((((size_t)x.b * a.T + x.t) * a.H + h) * a.W + w) * (size_t)a.c_out + x.n0;
       const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ab * a.n_tile);
-      for (int c = 0; c < a.n_tile / 32; ++c) {
+      for (int c = 0; c < a.n_tile / 32; ++c, ++nchunk) {
         uint32_t v[32];
         tmem_ld32(acc + static_cast<uint32_t>(c * 32), v);
         tmem_ld_wait_regs(v);
@@ -304,23 +333,31 @@ __global__ void __launch_bounds__(kConvThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&bar_acc_empty[ab]);
         }
-        if (inside) {
-          uint32_t pk[16];
+        const float bl = a.bias ? a.bias[x.n0 + c * 32 + lane] : 0.f;
+        uint32_t pk[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            float lo = __uint_as_float(v[2 * k]), hi2 = __uint_as_float(v[2 * k + 1]);
-            if (a.bias) {
-              lo += a.bias[x.n0 + c * 32 + 2 * k];
-              hi2 += a.bias[x.n0 + c * 32 + 2 * k + 1];
-            }
-            pk[k] = pack_bf16x2(lo, hi2);
-          }
-          uint4* o = reinterpret_cast<uint4*>(dst + c * 32);
+        for (int k = 0; k < 16; ++k) {
+          const float lo = __uint_as_float(v[2 * k]) + __shfl_sync(0xffffffffu, bl, 2 * k);
+          const float hi2 = __uint_as_float(v[2 * k + 1]) + __shfl_sync(0xffffffffu, bl, 2 * k + 1);
+          pk[k] = pack_bf16x2(lo, hi2);
+        }
+        uint8_t* st = stage0 + (nchunk & 1) * kOutStage;
+        // This buffer's previous store (two chunks back) must have read it.
+        if (leader) bulk_wait_group_read<1>();
+        named_bar_sync(1, 128);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) o[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(st + sw64_offset(r, j)) = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2],
+                                                                          pk[4 * j + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (leader) {
+          tma_store_5d(&tm_y, st, x.n0 + c * 32, x.w0, x.h0, x.t, x.b);
+          bulk_commit_group();
         }
       }
     }
+    if (leader) bulk_wait_group0();
   }
 
   tc_fence_before();
@@ -401,11 +438,12 @@ int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const
     return WAN_ERR_CUDA;
   const int grid = (int)(total < sms ? total : sms);  // persistent: one CTA per SM
 
-  CUtensorMap tx, tc, tw;
+  CUtensorMap tx, tc, tw, ty;
   const int cache_frames = time_down ? 1 : 2;
   if (!make_tmap_act(&tx, x, B, T, H, W, c_in, kc) ||
       !make_tmap_act(&tc, cache ? cache : x, B, cache ? cache_frames : T, H, W, c_in, kc) ||
-      !make_tmap_wt(&tw, wt, c_in, c_out, time_down ? 3 : 27, n_tile, kc))
+      !make_tmap_wt(&tw, wt, c_in, c_out, time_down ? 3 : 27, n_tile, kc) ||
+      !make_tmap_act(&ty, y, B, a.T, H, W, c_out, 32))  // output: boxes of 32 channels, 64-byte swizzle
     return WAN_ERR_CUDA;
   auto kern = time_down ? (kc == 64 ? causal_conv3d_kernel<64, true> : causal_conv3d_kernel<32, true>)
                         : (kc == 64 ? causal_conv3d_kernel<64, false> : causal_conv3d_kernel<32, false>);
@@ -413,7 +451,7 @@ int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return WAN_ERR_CUDA;
   record_start(lc, s);
-  kern<<<grid, kConvThreads, smem, s>>>(tx, tc, tw, a);
+  kern<<<grid, kConvThreads, smem, s>>>(tx, tc, tw, ty, a);
   record_stop(lc, s);
   return cudaGetLastError() == cudaSuccess ? WAN_OK : WAN_ERR_CUDA;
 }
