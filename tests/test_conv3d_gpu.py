@@ -51,6 +51,7 @@ def _run(x, cache, wt, bias, cache_out=True, stream=None):
     (1, 3, 8, 16, 32, 64, False, True),      # C_in 32: one K step per tap
     (2, 1, 5, 33, 160, 224, True, False),    # C_in 160 = 5 x 32, N = 224
     (1, 2, 7, 18, 96, 320, True, True),      # 32-channel K steps, N = 64 x 5
+    (1, 2, 9, 17, 64, 32, True, True),       # C_out 32: one 32-channel store per tile, ragged
 ])
 def test_conv3d_every_output(B, T, H, W, c_in, c_out, with_cache, with_bias):
     x, cache, wt, bias = _layer(21, B, T, H, W, c_in, c_out, with_cache, with_bias)
