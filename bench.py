@@ -124,14 +124,16 @@ class ClockSampler:
 # Distributed plumbing (timing only: barrier and max over ranks)
 
 
-def dist_setup(n_gpus: int):
+def dist_setup(n_gpus: int, gpu: bool = True):
+    """Process group for N > 1 ranks: NCCL for the GPU arm, gloo for the
+    reference arm (which runs on the host cores and needs no GPU)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
 
-        backend = os.environ.get("WAN_BENCH_BACKEND", "nccl")
+        backend = os.environ.get("WAN_BENCH_BACKEND", "nccl" if gpu else "gloo")
         if backend == "nccl":
             import torch
 
@@ -1017,7 +1019,7 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
-    rank, world, local = dist_setup(args.gpus)
+    rank, world, local = dist_setup(args.gpus, gpu=args.impl != "reference")
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
