@@ -264,6 +264,25 @@ def _head_backward(qr_rows, do_rows, kr, vh, scale, block, need_dkdv=True):
     return dqr, dkr, dv
 
 
+def head_backward_given_o_lse(qr_rows, do_rows, kr, vh, o_rows, lse_rows, scale):
+    """Gradients of one head as the backward entry point defines them: from the
+    forward's outputs rather than recomputed ones.
+
+    The backward is handed O and LSE by the forward; the softmax weights are
+    P_ij = exp(scale * qr_i . kr_j - LSE_i) and the row term is
+    D_i = dO_i . O_i with that O (gojay.top reading, section 3 Training: the
+    gradient of the softmax through dS = P o (dP - D)). With the exact O and
+    LSE this is _head_backward; with rounded ones it is the backward of the
+    values a training step actually passes on.
+    Returns dQ_rot [m, d], dK_rot [n, d], dV [n, d].
+    """
+    s = scale * (qr_rows @ kr.T)
+    p = np.exp(s - lse_rows[:, None])
+    d_i = np.sum(do_rows * o_rows, axis=1, keepdims=True)
+    ds = p * (do_rows @ vh.T - d_i)
+    return scale * (ds @ kr), scale * (ds.T @ qr_rows), p.T @ do_rows
+
+
 def self_attention_bwd(q, k, v, dout, grid, theta=DEFAULT_THETA, scale=None, block=1024):
     """dQ, dK, dV [B, L, H, d] of sum(O * dout) for 3D-RoPE self-attention.
 

@@ -380,6 +380,45 @@ def test_backward_sum_invariants():
     assert all(np.all(g == 0) for g in z)
 
 
+def test_backward_given_o_lse_equals_the_backward_with_exact_outputs():
+    """With the exact O and LSE, the backward from given outputs is the
+    backward that recomputes them (P = exp(s - LSE) is the softmax)."""
+    m, n, d, scale = 24, 40, 16, 0.3
+    qr, kr, vh, do = (RNG.standard_normal(sh) for sh in ((m, d), (n, d), (n, d), (m, d)))
+    o, lse = ref.softmax_attention(qr, kr, vh, scale)
+    got = ref.head_backward_given_o_lse(qr, do, kr, vh, o, lse, scale)
+    want = ref._head_backward(qr, do, kr, vh, scale, 7)
+    for g, w in zip(got, want):
+        np.testing.assert_allclose(g, w, rtol=1e-10, atol=1e-12)
+
+
+def test_backward_given_o_lse_uses_the_given_outputs():
+    """A perturbed O row i moves only D_i: dQ_rot_i shifts by
+    -scale (dO_i . delta) sum_j P_ij k_j, dK_rot_j by -scale (dO_i . delta) P_ij q_i,
+    dV not at all. A shifted LSE row i scales that row's P, so its dQ_rot by e^-c."""
+    m, n, d, scale = 6, 9, 8, 0.7
+    qr, kr, vh, do = (RNG.standard_normal(sh) for sh in ((m, d), (n, d), (n, d), (m, d)))
+    o, lse = ref.softmax_attention(qr, kr, vh, scale)
+    base = ref.head_backward_given_o_lse(qr, do, kr, vh, o, lse, scale)
+    p = np.exp(scale * (qr @ kr.T) - lse[:, None])
+    i, delta = 2, RNG.standard_normal(d)
+    o2 = o.copy()
+    o2[i] += delta
+    got = ref.head_backward_given_o_lse(qr, do, kr, vh, o2, lse, scale)
+    c = float(do[i] @ delta)
+    want_dq = base[0].copy()
+    want_dq[i] -= scale * c * (p[i] @ kr)
+    want_dk = base[1] - scale * c * np.outer(p[i], qr[i])
+    np.testing.assert_allclose(got[0], want_dq, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(got[1], want_dk, rtol=1e-10, atol=1e-12)
+    np.testing.assert_array_equal(got[2], base[2])
+    lse2 = lse.copy()
+    lse2[i] += 0.75
+    got = ref.head_backward_given_o_lse(qr, do, kr, vh, o, lse2, scale)
+    np.testing.assert_allclose(got[0][i], np.exp(-0.75) * base[0][i], rtol=1e-10)
+    np.testing.assert_allclose(np.delete(got[0], i, axis=0), np.delete(base[0], i, axis=0), rtol=1e-12)
+
+
 def test_flop_convention():
     assert ref.attention_flops(1, 40, 75600, 75600, 128) == pytest.approx(1.1705e14, rel=1e-4)
     assert ref.attention_flops(1, 12, 32760, 32760, 128) == pytest.approx(6.594e12, rel=1e-3)
