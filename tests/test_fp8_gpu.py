@@ -120,6 +120,22 @@ def _run(qb, kb, vb, grid):
     return dev_to_f64(o), dev_to_f64(lse)
 
 
+@pytest.mark.parametrize("scale", [0.02, 0.25, 1.0])
+def test_fp8_other_scales_against_the_quantised_oracle(scale):
+    """The softmax scale is an argument: every row at scales other than
+    1/sqrt(128) against the quantised oracle at that scale, within the bound
+    its rounding model gives for that softmax (peaked rows at 1.0)."""
+    B, grid, H = 1, (4, 8, 8), 2
+    qb, kb, vb = _inputs(B, grid, H, 61)
+    o, lse = wan.attention_forward_fp8(to_dev(qb), to_dev(kb), to_dev(vb), grid, scale=scale)
+    wan.check(wan.wan_get_device_status())
+    o, lse = dev_to_f64(o), dev_to_f64(lse)
+    for h in range(H):
+        qd, kd, vd = fp8.head_operands(f64(qb[0, :, h]), f64(kb[0, :, h]), f64(vb[0, :, h]), grid)
+        o_q, lse_q, sig = quantised_reference(qd, kd, vd, logit_gain=scale * math.sqrt(128))
+        compare_fp8_quantised(o[0, :, h], lse[0, h], o_q, lse_q, sig, f"scale {scale}, h{h}")
+
+
 @pytest.mark.parametrize("B,grid,H", [
     (1, (3, 8, 8), 2),     # 192 tokens
     (1, (3, 7, 9), 2),     # 189: ragged key and query tiles
