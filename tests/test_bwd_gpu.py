@@ -40,6 +40,8 @@ SMALL = [
     (1, (8, 16, 16), 2),   # 2048: many tiles both ways
     (2, (5, 13, 17), 1),   # 1105: ragged, odd extents
     (1, (2, 4, 5), 72),    # 40 tokens, 72 heads: the row pass takes its heads in two passes (64 + 8)
+    (1, (1, 1, 1), 2),     # a single token
+    (3, (1, 1, 129), 3),   # 129 tokens in a 1 x 1 x W grid, B = 3: one row past a key tile
 ]
 
 

@@ -77,6 +77,8 @@ SMALL_GRIDS = [
     (1, (8, 16, 16), 2),   # 2048: many key tiles
     (2, (5, 13, 17), 1),   # 1105: ragged, odd extents
     (1, (1, 1, 1), 1),     # a single token
+    (3, (1, 1, 129), 5),   # 129 tokens in a 1 x 1 x W grid (t and h angles all 0), B = 3, H = 5
+    (1, (257, 1, 1), 2),   # 257 tokens along t only: one row past a 256-row query pair
 ]
 
 
