@@ -725,6 +725,35 @@ def _extra_tiny(wan, torch, dev, w, stream, out, iters=200):
     ker = statistics.median(x.elapsed_time(y) for x, y in ev) * 1e3
     out[w.name] = {"us_per_call": round(us, 2), "kernel_us_median": round(ker, 2),
                    "note": "back-to-back calls on one stream; latency-bound (192 tokens)"}
+    # The same call captured once in a CUDA graph and replayed: the device
+    # latency of the two kernels without the host's per-call work between them.
+    try:
+        def call_current():
+            wan.check(wan.wan_attn_fwd(q, k, v, o, lse, B, w.grid, H, d, tab, 1 / math.sqrt(d), ws, wsb))
+
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                call_current()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call_current()
+        for _ in range(20):
+            graph.replay()
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(iters):
+            graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        wan.check(wan.wan_get_device_status())
+        out[w.name]["graph_us_per_call"] = round(a.elapsed_time(b) / iters * 1e3, 2)
+    except Exception as e:  # report, do not fail the bench line
+        out[w.name]["graph_us_per_call"] = None
+        out[w.name]["graph_error"] = str(e)[:200]
 
 
 def _extra_480p(wan, torch, dev, w, stream, timeit, out):
