@@ -104,7 +104,10 @@ size_t wan_attn_workspace_size(int op, int B, wan_grid_t g, int H, int head_dim)
  *   tables  : device tables from wan_rope3d_tables for the same grid/head_dim
  *   scale   : logit scale (1/sqrt(128) for the Wan models)
  *   workspace, ws_bytes : device scratch of at least wan_attn_workspace_size(WAN_OP_FWD, ...)
- * B == 0 is a no-op returning WAN_OK.
+ * B == 0 is a no-op returning WAN_OK. The call only enqueues kernels on
+ * `stream` (no allocation, no synchronisation): after a first call on the
+ * device it can be captured in a CUDA graph, whose replays compute on the
+ * buffers' current contents.
  */
 int wan_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, wan_grid_t g, int H,
                  int head_dim, const float* tables, float scale, void* workspace, size_t ws_bytes,
