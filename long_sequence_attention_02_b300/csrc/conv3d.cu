@@ -82,8 +82,7 @@ struct ConvCfg {
 
 struct ConvArgs {
   const float* bias;     // [C_out] or null
-  __nv_bfloat16* y;      // [B, T, H, W, C_out]
-  int B, T, H, W, c_in, c_out, n_tile;
+  int B, T, H, W, c_in, c_out, n_tile;  // T: output frames (half the input's for time downsampling)
   int tiles_h, tiles_w, tiles_n;
   int n_tiles_total;     // B * tiles_h * tiles_w * T * tiles_n
   uint32_t tmem_cols;    // power of two >= 2 * n_tile
@@ -414,7 +413,6 @@ int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const
   const int kc = c_in % 64 == 0 ? 64 : 32;  // input channels per K step
   ConvArgs a;
   a.bias = bias;
-  a.y = static_cast<__nv_bfloat16*>(y);
   a.B = B;
   a.T = time_down ? T / 2 : T;  // output frames
   a.H = H;
