@@ -52,6 +52,13 @@ def _run(x, cache, wt, bias, cache_out=True, stream=None):
     (2, 1, 5, 33, 160, 224, True, False),    # C_in 160 = 5 x 32, N = 224
     (1, 2, 7, 18, 96, 320, True, True),      # 32-channel K steps, N = 64 x 5
     (1, 2, 9, 17, 64, 32, True, True),       # C_out 32: one 32-channel store per tile, ragged
+    # widths at (or near) a multiple of 128: tiles are 1 x 128 strips whose
+    # three kw taps share one 130-pixel input box
+    (1, 2, 3, 128, 64, 128, True, True),     # one strip per row
+    (1, 2, 4, 250, 64, 192, True, True),     # ragged last strip (122 of 128 pixels)
+    (2, 1, 3, 256, 96, 96, False, True),     # strips with 32-channel K steps, first chunk, B = 2
+    (1, 3, 2, 128, 128, 320, True, False),   # strips, N = 64 x 5
+    (1, 2, 3, 124, 64, 64, True, True),      # one strip wider than the picture
 ])
 def test_conv3d_every_output(B, T, H, W, c_in, c_out, with_cache, with_bias):
     x, cache, wt, bias = _layer(21, B, T, H, W, c_in, c_out, with_cache, with_bias)
@@ -79,6 +86,23 @@ def test_conv3d_chunks_through_the_cache_equal_the_whole_video():
     assert torch.equal(chunked, whole)
     y_ref, _ = vae.causal_conv3d(f64(x), f64(wt), bias.astype(np.float64))
     compare(dev_to_f64(chunked), y_ref, "chunked y")
+
+
+def test_conv3d_strip_chunks_through_the_cache_equal_the_whole_video():
+    """The same in strip tiles (width 128): chunks of 2, 1 and 3 frames."""
+    B, T, H, W, c_in, c_out = 1, 6, 3, 128, 64, 64
+    x, _, wt, bias = _layer(24, B, T, H, W, c_in, c_out, False, True)
+    xd = to_dev(x)
+    whole, _ = _run(xd, None, wt, bias)
+    outs, cache, t0 = [], None, 0
+    for n in (2, 1, 3):
+        y, cache = _run(xd[:, t0:t0 + n].contiguous(), cache, wt, bias)
+        outs.append(y)
+        t0 += n
+    chunked = torch.cat(outs, dim=1)
+    assert torch.equal(chunked, whole)
+    y_ref, _ = vae.causal_conv3d(f64(x), f64(wt), bias.astype(np.float64))
+    compare(dev_to_f64(chunked), y_ref, "chunked y (strips)")
 
 
 def test_conv3d_without_cache_output_on_a_side_stream():
@@ -113,9 +137,9 @@ def test_conv3d_full_size_sampled():
 
 def test_conv3d_timed_layer_sampled():
     """The layer the benchmark times (4 frames of 360 x 640, 192 -> 192
-    channels, with a cache: 45 x 40 output patches of 8 x 16 per frame) on
-    512 seeded sampled positions plus the corners and the edges of the last
-    patch row and column."""
+    channels, with a cache: 360 x 5 output strips of 128 pixels per frame) on
+    512 seeded sampled positions plus the corners, the last row and column,
+    and both sides of every strip boundary."""
     from long_sequence_attention_02_b300.workloads import CONV_WORKLOADS
 
     w = CONV_WORKLOADS["wan_vae_conv3d_360x640_192"]
@@ -130,6 +154,7 @@ def test_conv3d_timed_layer_sampled():
              (0, 1, H - 8, W - 16), (0, 2, H - 1, W - 17), (0, 3, H - 9, W - 1), (0, 0, 7, 15), (0, 0, 8, 16)]
     edges += [(0, t, H - 1, int(c)) for t in range(T) for c in rng.integers(0, W, 8)]
     edges += [(0, t, int(r), W - 1) for t in range(T) for r in rng.integers(0, H, 8)]
+    edges += [(0, int(rng.integers(T)), int(rng.integers(H)), w0 + d) for w0 in range(128, W, 128) for d in (-1, 0)]
     pos = edges + pos
     got = dev_to_f64(torch.stack([y[p] for p in pos]))
     ref = vae.causal_conv3d_at(f64(x), f64(wt), bias.astype(np.float64), f64(cache), pos)
@@ -166,6 +191,7 @@ def test_conv3d_96_channel_720p_layer_sampled():
     n = 512
     T, H, W = w.T, w.H, w.W
     pos = [(0, 0, 0, 0), (0, T - 1, H - 1, W - 1), (0, 0, H - 1, 0), (0, T - 1, 0, W - 1), (0, 1, H - 8, W - 16)]
+    pos += [(0, int(rng.integers(T)), int(rng.integers(H)), w0 + d) for w0 in range(128, W, 128) for d in (-1, 0)]
     pos += list(zip(rng.integers(0, w.B, n), rng.integers(0, T, n), rng.integers(0, H, n), rng.integers(0, W, n)))
     got = dev_to_f64(torch.stack([y[p] for p in pos]))
     ref = vae.causal_conv3d_at(f64(x), f64(wt), bias.astype(np.float64), f64(cache), pos)
