@@ -14,6 +14,8 @@
 // else the largest of 256, 192, 128, 64 and 32 that divides C_out. The
 // positions are a strip of 128 consecutive pixels of one image row when the
 // width is a multiple of 128 (or nearly so), else an 8 (h) x 16 (w) patch.
+// When N <= 128 a strip tile holds two strips (rows h0 and h0 + 1), each
+// with its own accumulator, so that every weight box feeds 256 positions.
 // Per K step (one tap, kc = 64 input channels, or 32 when C_in is not a
 // multiple of 64):
 // - A = the 128 input pixels that tap reads, kc channels each, from a 5D TMA
@@ -21,9 +23,10 @@
 //   padding, and, for a first chunk, the causal padding too (a negative frame
 //   coordinate). With a cache, taps that reach before the chunk read the cache
 //   tensor instead. For a strip, one box of 130 pixels (the strip and one
-//   pixel either side) serves the three taps kw = 0, 1, 2 of a row: the MMA
-//   descriptor of tap kw starts kw rows into it. The swizzle is a function of
-//   the shared-memory address, so a descriptor may start at any row.
+//   pixel either side; one such row per strip of the tile) serves the three
+//   taps kw = 0, 1, 2 of a row: the MMA descriptor of tap kw starts kw rows
+//   into it. The swizzle is a function of the shared-memory address, so a
+//   descriptor may start at any row.
 // - B = the tap's N x kc weights: one 3D box {kc c, 1 tap, N}.
 // Both land swizzled (rows of 2 kc bytes, 128- or 64-byte swizzle), and kc/16
 // tcgen05.mma of kind::f16 (K = 16 each) accumulate into TMEM.
@@ -90,7 +93,7 @@ struct ConvCfg {
 struct ConvArgs {
   const float* bias;     // [C_out] or null
   int B, T, H, W, c_in, c_out, n_tile;  // T: output frames (half the input's for time downsampling)
-  int ph, pw;            // positions of a tile: 1 x 128 (strip) or 8 x 16 (patch)
+  int ph, pw;            // positions of a tile: 1 or 2 x 128 (strips) or 8 x 16 (patch)
   int tiles_h, tiles_w, tiles_n;
   int n_tiles_total;     // B * tiles_h * tiles_w * T * tiles_n
   uint32_t tmem_cols;    // power of two >= 2 * n_tile
@@ -198,7 +201,10 @@ __device__ __forceinline__ uint64_t conv_desc(uint32_t saddr) {
 // kModeTimeDown selects the time-downsampling layer (Fig. vae_cache (b)):
 // 3 x 1 x 1 taps with stride 2 in time; output frame t reads frames 2t - 1,
 // 2t and 2t + 1 of the chunk, frame -1 being the one cached frame.
-enum ConvMode : int { kModePatch = 0, kModeStrip = 1, kModeTimeDown = 2 };
+// kModeStrip2 stacks two strips (image rows h0 and h0 + 1) in one tile, with
+// an accumulator each: a 2-row input box serves both, and each weight box
+// feeds both strips' MMAs (for N <= 128, so that 2 x 2 accumulators fit TMEM).
+enum ConvMode : int { kModePatch = 0, kModeStrip = 1, kModeTimeDown = 2, kModeStrip2 = 3 };
 
 template <int kC, int kMode>
 __global__ void __launch_bounds__(kConvThreads, 1)
@@ -221,8 +227,11 @@ __global__ void __launch_bounds__(kConvThreads, 1)
   volatile int* abort = &abort_sh;
   const uint64_t to = a.lc.timeout_ns;
   constexpr bool kTimeDown = kMode == kModeTimeDown;
-  constexpr bool kFused = kMode != kModeStrip;     // A and B of a step on one barrier
+  constexpr bool kStrip = kMode == kModeStrip || kMode == kModeStrip2;
+  constexpr bool kFused = !kStrip;                 // A and B of a step on one barrier
   constexpr int kTapsPerA = kFused ? 1 : 3;        // taps one A box serves
+  constexpr int kRows = kMode == kModeStrip2 ? 2 : 1;  // strips per tile, one accumulator each
+  constexpr uint32_t kBoxRowLo = 130 * Cfg::kRow >> 4;  // one 130-pixel input row, in descriptor units
   constexpr int kTaps = kTimeDown ? 3 : 27;
   const int c_steps = a.c_in / kC;
   const int a_steps = kTaps / kTapsPerA * c_steps;  // A boxes per tile
@@ -352,8 +361,8 @@ __global__ void __launch_bounds__(kConvThreads, 1)
     int i = 0;  // tiles of this CTA
     for (int idx = blockIdx.x; idx < a.n_tiles_total && ok; idx += gridDim.x, ++i) {
       const int ab = i & 1;
-      const uint32_t acc = tmem + static_cast<uint32_t>(ab * a.n_tile);
-      // The accumulator's previous tile has left TMEM.
+      const uint32_t acc = tmem + static_cast<uint32_t>(ab * kRows * a.n_tile);
+      // The accumulators' previous tile has left TMEM.
       if (i >= 2) {
         ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_empty[ab], ((i >> 1) - 1) & 1, abort, to));
         if (!ok) {
@@ -379,13 +388,16 @@ __global__ void __launch_bounds__(kConvThreads, 1)
             }
           }
           tc_fence_after();
-          // tap kw = j of a strip: the box's rows j .. j + 127
+          // tap kw = j of a strip: rows j .. j + 127 of the box's input row (one per strip)
           const uint32_t aj = a_lo + static_cast<uint32_t>(j * (Cfg::kRow >> 4));
           const int bslot = kFused ? pa.slot : pb.slot;  // for patches B came with A
           const uint32_t b_lo = lo0 + ((b_off + static_cast<uint32_t>(bslot) * b_stride) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kC / 16; ++kk)  // 16 channels (32 bytes) per MMA
-            umma_ss_elect_lo(acc, aj + kk * 2, b_lo + kk * 2, hi, idesc, (s > 0 || j > 0 || kk > 0) ? 1u : 0u);
+          for (int rr = 0; rr < kRows; ++rr)
+#pragma unroll
+            for (int kk = 0; kk < kC / 16; ++kk)  // 16 channels (32 bytes) per MMA
+              umma_ss_elect_lo(acc + static_cast<uint32_t>(rr * a.n_tile), aj + rr * kBoxRowLo + kk * 2,
+                               b_lo + kk * 2, hi, idesc, (s > 0 || j > 0 || kk > 0) ? 1u : 0u);
           if (!kFused) {
             umma_commit_elect(&b_empty[pb.slot]);
             pb.next(b_stages);
@@ -425,18 +437,28 @@ __global__ void __launch_bounds__(kConvThreads, 1)
       }
       tc_fence_after();
       const ConvTile x = conv_tile(idx, a);
-      const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ab * a.n_tile);
-      for (int c = 0; c < a.n_tile / 32; ++c, ++nchunk) {
+      const uint32_t acc =
+          tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ab * kRows * a.n_tile);
+      // Chunk c: TMEM columns 32c.. of the tile's accumulators, i.e. strip
+      // c / nch, output channels 32 (c % nch).. A second strip below the
+      // picture (odd H) is read but not stored.
+      const int nch = a.n_tile / 32;
+      for (int c = 0; c < kRows * nch; ++c) {
+        const int rr = kRows == 1 ? 0 : c / nch, cc = c - rr * nch;
+        const bool live = kRows == 1 || x.h0 + rr < a.H;  // the same for all four warps
         uint32_t v[32];
-        tmem_ld32(acc + static_cast<uint32_t>(c * 32), v);
-        tmem_ld_wait_regs(v);
-        if (c == a.n_tile / 32 - 1) {
-          // The accumulator may take the CTA's tile after next.
+        if (live) {
+          tmem_ld32(acc + static_cast<uint32_t>(c * 32), v);
+          tmem_ld_wait_regs(v);
+        }
+        if (c == kRows * nch - 1) {
+          // The accumulators may take the CTA's tile after next.
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bar_acc_empty[ab]);
         }
-        const float bl = a.bias ? a.bias[x.n0 + c * 32 + lane] : 0.f;
+        if (!live) continue;
+        const float bl = a.bias ? a.bias[x.n0 + cc * 32 + lane] : 0.f;
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -455,9 +477,10 @@ __global__ void __launch_bounds__(kConvThreads, 1)
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (leader) {
-          tma_store_5d(&tm_y, st, x.n0 + c * 32, x.w0, x.h0, x.t, x.b);
+          tma_store_5d(&tm_y, st, x.n0 + cc * 32, x.w0, x.h0 + rr, x.t, x.b);
           bulk_commit_group();
         }
+        ++nchunk;
       }
     }
     if (leader) bulk_wait_group0();
@@ -524,6 +547,7 @@ int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const
   const int kc = c_in % 64 == 0 ? 64 : 32;  // input channels per K step
   const uint32_t row = static_cast<uint32_t>(kc * 2);
   const bool strip = conv3d_uses_strips(W, time_down);
+  const int rows = strip && 4 * n_tile <= 512 ? 2 : 1;  // strips per tile (2 x rows accumulators in TMEM)
   ConvArgs a;
   a.bias = bias;
   a.B = B;
@@ -533,7 +557,7 @@ int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const
   a.c_in = c_in;
   a.c_out = c_out;
   a.n_tile = n_tile;
-  a.ph = strip ? 1 : 8;
+  a.ph = strip ? rows : 8;
   a.pw = strip ? 128 : 16;
   a.tiles_h = (H + a.ph - 1) / a.ph;
   a.tiles_w = (W + a.pw - 1) / a.pw;
@@ -542,7 +566,7 @@ int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const
   a.lc = lc;
   // Rings: a strip's A box (130 rows) serves three taps, so its ring is short
   // and B takes the rest; a patch's A and B advance together in {A, B} stages.
-  const int a_rows = strip ? a.pw + 2 : 128;
+  const int a_rows = strip ? (a.pw + 2) * rows : 128;
   a.a_bytes = static_cast<uint32_t>(a_rows) * row;
   const uint32_t a_slot = round_up_1k(a.a_bytes);
   const uint32_t b_slot = static_cast<uint32_t>(n_tile) * row;  // n_tile % 32 == 0: a multiple of 1024
@@ -563,7 +587,8 @@ int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const
   if (a.a_stages < 1 || a.b_stages < 2) return WAN_ERR_UNSUPPORTED;
   const int smem = static_cast<int>(a.out_off) + 2 * kOutStage + 1024;
   // Two accumulators of n_tile fp32 columns; TMEM is allocated in powers of two.
-  a.tmem_cols = 2 * n_tile <= 128 ? 128u : (2 * n_tile <= 256 ? 256u : 512u);
+  const int cols = 2 * rows * n_tile;
+  a.tmem_cols = cols <= 128 ? 128u : (cols <= 256 ? 256u : 512u);
   const long long total = (long long)B * a.T * a.tiles_h * a.tiles_w * a.tiles_n;
   if (total > INT_MAX) return WAN_ERR_INVALID;
   a.n_tiles_total = (int)total;
@@ -575,13 +600,16 @@ int launch_causal_conv3d(const void* x, const void* cache, const void* wt, const
 
   CUtensorMap tx, tc, tw, ty;
   const int cache_frames = time_down ? 1 : 2;
-  if (!make_tmap_act(&tx, x, B, T, H, W, c_in, kc, a_rows == 128 ? a.pw : a_rows, a.ph) ||
-      !make_tmap_act(&tc, cache ? cache : x, B, cache ? cache_frames : T, H, W, c_in, kc,
-                     a_rows == 128 ? a.pw : a_rows, a.ph) ||
+  // input box: {kc, 130, rows} for strips, {kc, 16, 8} for patches; output
+  // box: 32 channels of one strip or patch, 64-byte swizzle
+  const int in_w = strip ? a.pw + 2 : a.pw;
+  if (!make_tmap_act(&tx, x, B, T, H, W, c_in, kc, in_w, a.ph) ||
+      !make_tmap_act(&tc, cache ? cache : x, B, cache ? cache_frames : T, H, W, c_in, kc, in_w, a.ph) ||
       !make_tmap_wt(&tw, wt, c_in, c_out, time_down ? 3 : 27, n_tile, kc) ||
-      !make_tmap_act(&ty, y, B, a.T, H, W, c_out, 32, a.pw, a.ph))  // output: 32 channels, 64-byte swizzle
+      !make_tmap_act(&ty, y, B, a.T, H, W, c_out, 32, a.pw, strip ? 1 : a.ph))
     return WAN_ERR_CUDA;
   auto kern = time_down ? (kc == 64 ? causal_conv3d_kernel<64, kModeTimeDown> : causal_conv3d_kernel<32, kModeTimeDown>)
+              : rows == 2 ? (kc == 64 ? causal_conv3d_kernel<64, kModeStrip2> : causal_conv3d_kernel<32, kModeStrip2>)
               : strip   ? (kc == 64 ? causal_conv3d_kernel<64, kModeStrip> : causal_conv3d_kernel<32, kModeStrip>)
                         : (kc == 64 ? causal_conv3d_kernel<64, kModePatch> : causal_conv3d_kernel<32, kModePatch>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)

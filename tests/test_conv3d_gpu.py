@@ -53,12 +53,17 @@ def _run(x, cache, wt, bias, cache_out=True, stream=None):
     (1, 2, 7, 18, 96, 320, True, True),      # 32-channel K steps, N = 64 x 5
     (1, 2, 9, 17, 64, 32, True, True),       # C_out 32: one 32-channel store per tile, ragged
     # widths at (or near) a multiple of 128: tiles are 1 x 128 strips whose
-    # three kw taps share one 130-pixel input box
-    (1, 2, 3, 128, 64, 128, True, True),     # one strip per row
-    (1, 2, 4, 250, 64, 192, True, True),     # ragged last strip (122 of 128 pixels)
-    (2, 1, 3, 256, 96, 96, False, True),     # strips with 32-channel K steps, first chunk, B = 2
-    (1, 3, 2, 128, 128, 320, True, False),   # strips, N = 64 x 5
-    (1, 2, 3, 124, 64, 64, True, True),      # one strip wider than the picture
+    # three kw taps share one 130-pixel input box; with N <= 128 a tile
+    # stacks two strips (rows h0, h0 + 1), the second below the picture when
+    # H is odd
+    (1, 2, 3, 128, 64, 128, True, True),     # two strips per tile, one tile per row pair, odd H
+    (1, 2, 4, 250, 64, 192, True, True),     # one strip per tile (N = 192), ragged last strip (122 of 128)
+    (1, 2, 3, 128, 64, 256, True, True),     # one strip per tile, N = 256
+    (1, 1, 5, 250, 128, 160, False, True),   # one strip per tile, N = 160, ragged, first chunk
+    (2, 1, 3, 256, 96, 96, False, True),     # two strips, 32-channel K steps, first chunk, B = 2
+    (1, 3, 2, 128, 128, 320, True, False),   # two strips, N = 64 x 5
+    (1, 2, 3, 124, 64, 64, True, True),      # two strips wider than the picture
+    (1, 2, 1, 256, 32, 32, True, True),      # two strips, H = 1: every second strip below the picture
 ])
 def test_conv3d_every_output(B, T, H, W, c_in, c_out, with_cache, with_bias):
     x, cache, wt, bias = _layer(21, B, T, H, W, c_in, c_out, with_cache, with_bias)
@@ -89,7 +94,7 @@ def test_conv3d_chunks_through_the_cache_equal_the_whole_video():
 
 
 def test_conv3d_strip_chunks_through_the_cache_equal_the_whole_video():
-    """The same in strip tiles (width 128): chunks of 2, 1 and 3 frames."""
+    """The same in two-strip tiles (width 128, N = 64): chunks of 2, 1 and 3 frames."""
     B, T, H, W, c_in, c_out = 1, 6, 3, 128, 64, 64
     x, _, wt, bias = _layer(24, B, T, H, W, c_in, c_out, False, True)
     xd = to_dev(x)
