@@ -94,14 +94,19 @@ def test_timeout_in_fp8_forward():
     compare(dev_to_f64(lse), lse_ref, "fp8 LSE after recovery", max_abs=0.2, rel_l2=float("inf"))
 
 
-def test_timeout_in_conv3d():
-    """The VAE Conv3d producer withholds one K step: the MMA warp's bounded
-    wait expires, the epilogue skips its stores, TMEM is freed, and the next
-    call is correct."""
+@pytest.mark.parametrize("W,c_out", [
+    (16, 128),    # 8 x 16 patches: A and B of a K step on one barrier
+    (128, 192),   # 1 x 128 strips (N = 192): input and weight rings with producers of their own
+    (128, 64),    # two strips per tile (N = 64)
+])
+def test_timeout_in_conv3d(W, c_out):
+    """The VAE Conv3d's input producer withholds one box: the MMA warp's
+    bounded wait expires, the weight producer and the epilogue stop on the
+    abort flag, TMEM is freed, and the next call is correct."""
     from oracle import vae
     from tests._util import bf16_round
 
-    B, T, H, W, c_in, c_out = 1, 2, 8, 16, 64, 128
+    B, T, H, c_in = 1, 2, 8, 64
     x = bits(11, synth.STREAM_Q, (B, T, H, W, c_in))
     wt = bf16_round(f64(bits(11, synth.STREAM_V, (c_out, 3, 3, 3, c_in))) * 2.0 ** -5)
     xd, wd = to_dev(x), to_dev(wt)
