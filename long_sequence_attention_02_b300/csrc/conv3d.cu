@@ -35,8 +35,9 @@
 // their own, since an A box may serve three taps), 1 MMA issuer and TMEM
 // owner, 2-5 epilogue (TMEM -> + bias -> bf16 -> shared memory -> TMA stores
 // of 32 channels, which write only the positions inside the picture).
-// The CTAs are persistent (one per SM) and keep two accumulators in TMEM,
-// so that one tile's epilogue runs under the next tile's MMAs.
+// The CTAs are persistent (one per SM) and keep two sets of accumulators in
+// TMEM (one accumulator per strip of a tile), so that one tile's epilogue
+// runs under the next tile's MMAs.
 // Every wait is bounded; on a timeout the device error word is set.
 //
 // The same kernel, instantiated for kModeTimeDown, runs the encoder's
@@ -96,7 +97,7 @@ struct ConvArgs {
   int ph, pw;            // positions of a tile: 1 or 2 x 128 (strips) or 8 x 16 (patch)
   int tiles_h, tiles_w, tiles_n;
   int n_tiles_total;     // B * tiles_h * tiles_w * T * tiles_n
-  uint32_t tmem_cols;    // power of two >= 2 * n_tile
+  uint32_t tmem_cols;    // power of two >= 2 x (strips per tile) x n_tile
   int has_cache;
   // Rings in shared memory: A slot k at k * a_stride, B slot k at b_off +
   // k * b_stride, the two output staging buffers at out_off; all multiples
